@@ -1,0 +1,176 @@
+/*
+ * ssmscan.h — C ABI of libssmscan.so: the selective-scan (Mamba) and SSD (Mamba-2)
+ * forward passes on one NVIDIA B300 (sm_103a).
+ *
+ * Conventions for every entry point
+ *  - Pointers in the params structs are DEVICE pointers owned by the caller; the library
+ *    never allocates, frees or keeps them after the call returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Work is
+ *    enqueued on it and the call returns without synchronising (except ssm_workspace_status).
+ *  - Argument errors are detected on the host before anything is launched and return
+ *    SSM_ERR_INVALID_ARG (shape, stride, pointer, dtype or alignment problem) or
+ *    SSM_ERR_UNSUPPORTED (a valid request this build does not implement); a one-line
+ *    reason is then available from ssm_last_error() on the calling thread.
+ *  - A failed launch returns SSM_ERR_CUDA; the CUDA error string is in ssm_last_error().
+ *  - Stateless and thread-safe: calls on different streams may run concurrently as long
+ *    as their output and workspace buffers do not overlap.
+ *  - Arithmetic: inputs in the I/O dtype (fp32 or bf16) are widened to fp32; the state and
+ *    every intermediate are fp32; y is rounded to the I/O dtype (round to nearest even).
+ *
+ * Notation follows the pages: b batch, L sequence length, D channels (d_inner), N state
+ * size (d_state); for SSD H heads, P head dimension, G groups of (B, C), Q chunk length.
+ */
+#ifndef SSMSCAN_H
+#define SSMSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSMSCAN_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define SSMSCAN_API __attribute__((visibility("default")))
+#else
+#define SSMSCAN_API
+#endif
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1,
+    SSM_ERR_UNSUPPORTED = 2,
+    SSM_ERR_CUDA = 3,
+    SSM_ERR_TIMEOUT = 4,   /* a bounded device-side wait gave up (see ssm_workspace_status) */
+    SSM_ERR_WORKSPACE = 5  /* workspace missing, too small or misaligned */
+} ssm_status_t;
+
+typedef enum { SSM_DTYPE_F32 = 0, SSM_DTYPE_BF16 = 1 } ssm_dtype_t;
+
+/* How B_bar x is formed from delta, A and B.
+ * SSM_DISC_DELTA_B: B_bar x = delta * B * x, the simplified discretisation of every
+ *   selective listing on the pages ("Mamba/SSM complete guide" section 5 `selective_scan`,
+ *   einsum "bld,bln,bld->bldn"; "State Space Model / Mamba", "Mamba風の選択的SSMの実装").
+ * SSM_DISC_ZOH: exact zero-order hold for diagonal A, B_bar = (exp(delta a) - 1) / a * B
+ *   ("State Space Model / Mamba", "Zero-Order Hold" and `discretize_zoh`; "Mamba/SSM
+ *   complete guide" section 2 ZOH formula), with the limit delta * B where a == 0. */
+typedef enum { SSM_DISC_DELTA_B = 0, SSM_DISC_ZOH = 1 } ssm_discretization_t;
+
+/*
+ * Mamba-1 selective scan, one independent recurrence per (batch, channel):
+ *   dt_t   = softplus(delta[b,t,d] + delta_bias[d])      (softplus(v) = log(1 + e^v))
+ *   A_bar  = exp(dt_t * A[d,n])
+ *   h[n]   = A_bar * h[n] + dt_t * B[b,t,n] * x[b,t,d]    (or the ZOH form above)
+ *   y      = sum_n C[b,t,n] * h[n]  +  D[d] * x[b,t,d]
+ *   y     *= silu(z[b,t,d]) = z / (1 + e^-z)
+ * The output at t reads the state after x_t has entered it. The state starts at h0
+ * (zeros when NULL) and its value after the last step is written to h_last.
+ * Pages: "Mamba/SSM complete guide" section 5, listing `selective_scan` (discretise, loop,
+ * readout, u*D) and MambaBlock.forward (y * silu(z)); "論文解説: Mamba" "選択機構"
+ * (softplus) and "Hardware-Aware Parallel Scan" (the recurrence, zero initial state).
+ */
+typedef struct ssm_scan_params {
+    int64_t batch;          /* b >= 1 */
+    int64_t seqlen;         /* L >= 0 (L == 0: nothing is launched except copying h0 to h_last) */
+    int64_t dim;            /* D >= 1 */
+    int64_t dstate;         /* N, 1 <= N <= 256 */
+    int32_t io_dtype;       /* ssm_dtype_t of x, delta, z, B, C and y */
+    int32_t delta_softplus; /* 1: dt = softplus(delta + bias); 0: dt = delta + bias */
+    int32_t reverse;        /* 1: run t = L-1 .. 0 (h_last is then the state after t = 0) */
+    int32_t discretization; /* ssm_discretization_t */
+    const void* x;          /* (b, L, D), strides x_stride */
+    const void* delta;      /* (b, L, D), strides delta_stride; a channel stride of 0 gives
+                               one delta per token shared by all channels */
+    const void* B;          /* (b, L, N), strides B_stride, shared by all channels */
+    const void* C;          /* (b, L, N), strides C_stride, shared by all channels */
+    const void* z;          /* (b, L, D) or NULL (no gate), strides z_stride */
+    const float* A;         /* (D, N) fp32, contiguous; expected <= 0 (not enforced) */
+    const float* D;         /* (D) fp32 or NULL (no skip) */
+    const float* delta_bias;/* (D) fp32 or NULL (zero bias) */
+    const float* h0;        /* (b, D, N) fp32 contiguous, or NULL (zeros) */
+    void* y;                /* (b, L, D) in io_dtype, strides y_stride; must not alias inputs */
+    float* h_last;          /* (b, D, N) fp32 contiguous, or NULL (not written) */
+    int64_t x_stride[3];    /* element strides for (b, t, d); 0 broadcasts */
+    int64_t delta_stride[3];
+    int64_t z_stride[3];
+    int64_t y_stride[3];    /* y must not broadcast: all strides > 0 unless the size is 1 */
+    int64_t B_stride[3];    /* (b, t, n) */
+    int64_t C_stride[3];
+    int64_t chunk_len;      /* time-chunk length for the chunk-carry path; 0 = choose */
+    void* workspace;        /* device scratch of ssm_scan_workspace_size() bytes, 256-byte
+                               aligned; may be NULL when that size is 0 */
+    size_t workspace_bytes;
+} ssm_scan_params;
+
+/* Bytes of device workspace ssm_scan_fwd needs for these params (0 if none). Host only,
+ * no CUDA call. Returns (size_t)-1 when the params are invalid. */
+SSMSCAN_API size_t ssm_scan_workspace_size(const ssm_scan_params* p);
+
+/* Enqueue the selective scan on `stream`. Returns SSM_OK once launched. */
+SSMSCAN_API ssm_status_t ssm_scan_fwd(const ssm_scan_params* p, void* stream);
+
+/*
+ * Mamba-2 SSD chunked scan: the same recurrence with one scalar A per head and the state
+ * an N x P matrix per (batch, head):
+ *   dt_t = softplus(delta[b,t,h] + delta_bias[h]);  S = exp(dt_t A_h) S + dt_t B_t (x) x_t
+ *   y_t  = S^T C_t (+ D_h x_t) (* silu(z_t))
+ * computed chunk by chunk (Q steps): inside a chunk by matrix products over the masked,
+ * decayed C B^T block, across chunks by handing the state on.
+ * Pages: "Mamba-2 / Structured State Space Duality" (abeam) "基本アイデア" (semiseparable
+ * matrix, block decomposition: diagonal blocks as block products, off-diagonal blocks as a
+ * low-rank state hand-off) and "線形形式と二次形式を使い分ける"; "Mamba/SSM complete guide"
+ * section 6 "SSD演算の概念" (intra-chunk matrix products, inter-chunk recurrence) and
+ * `Mamba2Block` (A per head; B, C of d_state each in in_proj).
+ * All tensors are dense and contiguous in the shapes below.
+ */
+typedef struct ssd_scan_params {
+    int64_t batch;          /* b >= 1 */
+    int64_t seqlen;         /* L >= 0 */
+    int64_t nheads;         /* H >= 1 */
+    int64_t headdim;        /* P */
+    int64_t dstate;         /* N */
+    int64_t ngroups;        /* G >= 1, divides H; head h reads group h / (H / G) */
+    int64_t chunk_size;     /* Q; the result does not depend on it beyond rounding */
+    int32_t io_dtype;       /* ssm_dtype_t of x, delta, B, C, z and y */
+    int32_t delta_softplus; /* as for ssm_scan_params */
+    const void* x;          /* (b, L, H, P) */
+    const void* delta;      /* (b, L, H) */
+    const float* A;         /* (H) fp32 */
+    const void* B;          /* (b, L, G, N) */
+    const void* C;          /* (b, L, G, N) */
+    const float* D;         /* (H) fp32 or NULL */
+    const void* z;          /* (b, L, H, P) or NULL */
+    const float* delta_bias;/* (H) fp32 or NULL */
+    const float* h0;        /* (b, H, N, P) fp32 or NULL */
+    void* y;                /* (b, L, H, P) in io_dtype */
+    float* h_last;          /* (b, H, N, P) fp32 or NULL */
+    void* workspace;        /* device scratch, 256-byte aligned */
+    size_t workspace_bytes;
+} ssd_scan_params;
+
+/* Bytes of device workspace ssd_chunk_scan_fwd needs (0 if none); (size_t)-1 if invalid. */
+SSMSCAN_API size_t ssd_chunk_scan_workspace_size(const ssd_scan_params* p);
+
+/* Enqueue the SSD chunked scan on `stream`. Returns SSM_OK once launched. */
+SSMSCAN_API ssm_status_t ssd_chunk_scan_fwd(const ssd_scan_params* p, void* stream);
+
+/* Synchronise `stream`, then report the device-side status word a kernel latched in
+ * `workspace` (SSM_OK, or SSM_ERR_TIMEOUT when a bounded wait gave up). `workspace` must be
+ * the buffer passed to the last call on that stream. NULL workspace reports SSM_OK. */
+SSMSCAN_API ssm_status_t ssm_workspace_status(const void* workspace, void* stream);
+
+/* Static, human-readable name of a status code. */
+SSMSCAN_API const char* ssm_status_string(ssm_status_t s);
+
+/* The reason for the last non-OK status returned on the calling thread ("" if none). */
+SSMSCAN_API const char* ssm_last_error(void);
+
+/* SSMSCAN_ABI_VERSION of the library that was loaded. */
+SSMSCAN_API int ssm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSMSCAN_H */

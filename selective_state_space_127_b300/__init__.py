@@ -1,0 +1,10 @@
+"""B300-native selective-scan (Mamba) and SSD (Mamba-2) forward passes.
+
+The compute lives in libssmscan.so (CUDA for sm_103a, C ABI in include/ssmscan.h); this
+package holds its build script, a ctypes binding and the seeded input generators.
+"""
+from .binding import (SSMError, load_library, ssd_chunk_scan_fwd, ssm_scan_fwd, ssm_scan_fwd_host,
+                      workspace_status)
+
+__all__ = ["SSMError", "load_library", "ssm_scan_fwd", "ssd_chunk_scan_fwd", "ssm_scan_fwd_host",
+           "workspace_status"]

@@ -1,0 +1,270 @@
+"""Python binding of libssmscan.so: argument marshalling only.
+
+Every step of the scan runs in the library's CUDA kernels; this module checks tensor
+placement and dtypes, fills the C params structs declared in include/ssmscan.h, allocates
+outputs and workspace with PyTorch (which owns device memory and streams) and calls the
+C ABI on the current torch stream. There is no CPU or PyTorch fallback: if the library is
+missing or a call fails, an exception says why.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libssmscan.so")
+
+SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_WORKSPACE = range(6)
+SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
+SSM_DISC_DELTA_B, SSM_DISC_ZOH = 0, 1
+ABI_VERSION = 1
+
+# Every function the header declares (checked by the CPU test suite).
+EXPORTS = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssd_chunk_scan_workspace_size", "ssd_chunk_scan_fwd",
+           "ssm_workspace_status", "ssm_status_string", "ssm_last_error", "ssm_abi_version")
+
+_i64, _i32, _vp, _sz = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
+
+
+class ScanParams(ctypes.Structure):
+    _fields_ = [("batch", _i64), ("seqlen", _i64), ("dim", _i64), ("dstate", _i64),
+                ("io_dtype", _i32), ("delta_softplus", _i32), ("reverse", _i32), ("discretization", _i32),
+                ("x", _vp), ("delta", _vp), ("B", _vp), ("C", _vp), ("z", _vp),
+                ("A", _vp), ("D", _vp), ("delta_bias", _vp), ("h0", _vp), ("y", _vp), ("h_last", _vp),
+                ("x_stride", _i64 * 3), ("delta_stride", _i64 * 3), ("z_stride", _i64 * 3),
+                ("y_stride", _i64 * 3), ("B_stride", _i64 * 3), ("C_stride", _i64 * 3),
+                ("chunk_len", _i64), ("workspace", _vp), ("workspace_bytes", _sz)]
+
+
+class SSDParams(ctypes.Structure):
+    _fields_ = [("batch", _i64), ("seqlen", _i64), ("nheads", _i64), ("headdim", _i64), ("dstate", _i64),
+                ("ngroups", _i64), ("chunk_size", _i64), ("io_dtype", _i32), ("delta_softplus", _i32),
+                ("x", _vp), ("delta", _vp), ("A", _vp), ("B", _vp), ("C", _vp), ("D", _vp), ("z", _vp),
+                ("delta_bias", _vp), ("h0", _vp), ("y", _vp), ("h_last", _vp),
+                ("workspace", _vp), ("workspace_bytes", _sz)]
+
+
+class SSMError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(f"{_status_name(status)}: {message}")
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libssmscan.so (built in-tree by ``python -m selective_state_space_127_b300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it with "
+                                   "`python -m selective_state_space_127_b300.build` (there is no fallback)")
+            lib = ctypes.CDLL(path)
+            lib.ssm_scan_workspace_size.argtypes = [ctypes.POINTER(ScanParams)]
+            lib.ssm_scan_workspace_size.restype = _sz
+            lib.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanParams), _vp]
+            lib.ssm_scan_fwd.restype = ctypes.c_int
+            lib.ssd_chunk_scan_workspace_size.argtypes = [ctypes.POINTER(SSDParams)]
+            lib.ssd_chunk_scan_workspace_size.restype = _sz
+            lib.ssd_chunk_scan_fwd.argtypes = [ctypes.POINTER(SSDParams), _vp]
+            lib.ssd_chunk_scan_fwd.restype = ctypes.c_int
+            lib.ssm_workspace_status.argtypes = [_vp, _vp]
+            lib.ssm_workspace_status.restype = ctypes.c_int
+            lib.ssm_status_string.argtypes = [ctypes.c_int]
+            lib.ssm_status_string.restype = ctypes.c_char_p
+            lib.ssm_last_error.argtypes = []
+            lib.ssm_last_error.restype = ctypes.c_char_p
+            lib.ssm_abi_version.argtypes = []
+            lib.ssm_abi_version.restype = ctypes.c_int
+            if lib.ssm_abi_version() != ABI_VERSION:
+                raise RuntimeError(f"{path}: ABI version {lib.ssm_abi_version()} != {ABI_VERSION}")
+            _lib = lib
+    return _lib
+
+
+def _status_name(s: int) -> str:
+    return ["SSM_OK", "SSM_ERR_INVALID_ARG", "SSM_ERR_UNSUPPORTED", "SSM_ERR_CUDA", "SSM_ERR_TIMEOUT",
+            "SSM_ERR_WORKSPACE"][s] if 0 <= s <= 5 else f"status {s}"
+
+
+def _check(lib, status: int):
+    if status != SSM_OK:
+        raise SSMError(status, lib.ssm_last_error().decode(errors="replace"))
+
+
+def _io_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SSM_DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return SSM_DTYPE_BF16
+    raise TypeError(f"I/O tensors must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _strides3(t, n_expected_dims=3):
+    if t is None:
+        return (0, 0, 0)
+    if t.dim() != n_expected_dims:
+        raise ValueError(f"expected a {n_expected_dims}-d tensor, got shape {tuple(t.shape)}")
+    return tuple(int(s) for s in t.stride())
+
+
+def _f32_contig(name, t, shape, device):
+    if t is None:
+        return None
+    if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != tuple(shape) or t.device != device:
+        raise ValueError(f"{name} must be a contiguous float32 tensor of shape {tuple(shape)} on {device}")
+    return t
+
+
+def _stream_handle(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_softplus=True, h0=None,
+                 reverse=False, zoh=False, chunk_len=0, out=None, return_last_state=True, h_last=None,
+                 stream=None):
+    """Selective scan on the GPU. x, delta, z: (b, L, D); B, C: (b, L, N); A: (D, N) fp32;
+    D, delta_bias: (D) fp32; h0: (b, D, N) fp32. I/O tensors are fp32 or bf16 (all alike) and
+    may be strided (delta's channel stride may be 0). Returns (y, h_last or None)."""
+    lib = load_library()
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor (use ssm_scan_fwd_host for host buffers)")
+    dev = x.device
+    b, L, Dm = x.shape
+    N = A.shape[1]
+    io = _io_dtype(x)
+    for name, t, shp in (("delta", delta, (b, L, Dm)), ("B", B, (b, L, N)), ("C", C, (b, L, N)),
+                         ("z", z, (b, L, Dm))):
+        if t is None:
+            continue
+        if t.device != dev or t.dtype != x.dtype or tuple(t.shape) != shp:
+            raise ValueError(f"{name} must be {x.dtype} of shape {shp} on {dev}, got {t.dtype} "
+                             f"{tuple(t.shape)} on {t.device}")
+    _f32_contig("A", A, (Dm, N), dev)
+    _f32_contig("D", D, (Dm,), dev)
+    _f32_contig("delta_bias", delta_bias, (Dm,), dev)
+    _f32_contig("h0", h0, (b, Dm, N), dev)
+    y = out if out is not None else torch.empty((b, L, Dm), device=dev, dtype=x.dtype)
+    if y.dtype != x.dtype or tuple(y.shape) != (b, L, Dm) or y.device != dev:
+        raise ValueError("out has the wrong dtype, shape or device")
+    hl = h_last
+    if hl is None and return_last_state:
+        hl = torch.empty((b, Dm, N), device=dev, dtype=torch.float32)
+    _f32_contig("h_last", hl, (b, Dm, N), dev)
+    p = ScanParams()
+    p.batch, p.seqlen, p.dim, p.dstate = b, L, Dm, N
+    p.io_dtype, p.delta_softplus, p.reverse = io, int(bool(delta_softplus)), int(bool(reverse))
+    p.discretization = SSM_DISC_ZOH if zoh else SSM_DISC_DELTA_B
+    p.x, p.delta, p.B, p.C, p.z = _ptr(x), _ptr(delta), _ptr(B), _ptr(C), _ptr(z)
+    p.A, p.D, p.delta_bias, p.h0 = _ptr(A), _ptr(D), _ptr(delta_bias), _ptr(h0)
+    p.y, p.h_last = _ptr(y), _ptr(hl)
+    p.x_stride[:] = _strides3(x)
+    p.delta_stride[:] = _strides3(delta)
+    p.z_stride[:] = _strides3(z)
+    p.y_stride[:] = _strides3(y)
+    p.B_stride[:] = _strides3(B)
+    p.C_stride[:] = _strides3(C)
+    p.chunk_len = int(chunk_len)
+    ws_bytes = lib.ssm_scan_workspace_size(ctypes.byref(p))
+    if ws_bytes == ctypes.c_size_t(-1).value:
+        _check(lib, lib.ssm_scan_fwd(ctypes.byref(p), None))  # raises with the reason
+    ws = None
+    if ws_bytes > 0:
+        ws = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+        p.workspace, p.workspace_bytes = _ptr(ws), ws_bytes
+    with torch.cuda.device(dev):
+        _check(lib, lib.ssm_scan_fwd(ctypes.byref(p), _stream_handle(stream)))
+    return y, hl
+
+
+def ssd_chunk_scan_fwd(x, delta, A, B, C, chunk_size=256, D=None, z=None, delta_bias=None, *,
+                       delta_softplus=True, h0=None, out=None, return_last_state=True, h_last=None,
+                       stream=None):
+    """SSD chunked scan on the GPU. x, z: (b, L, H, P); delta: (b, L, H); A, D, delta_bias: (H)
+    fp32; B, C: (b, L, G, N) or (b, L, N); h0: (b, H, N, P) fp32. Contiguous tensors only.
+    Returns (y, h_last or None)."""
+    lib = load_library()
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    dev = x.device
+    if B.dim() == 3:
+        B, C = B.unsqueeze(2), C.unsqueeze(2)
+    b, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    io = _io_dtype(x)
+    for name, t, shp in (("x", x, (b, L, H, P)), ("delta", delta, (b, L, H)), ("B", B, (b, L, G, N)),
+                         ("C", C, (b, L, G, N)), ("z", z, (b, L, H, P))):
+        if t is None:
+            continue
+        if t.device != dev or t.dtype != x.dtype or tuple(t.shape) != shp or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {x.dtype} tensor of shape {shp} on {dev}")
+    _f32_contig("A", A, (H,), dev)
+    _f32_contig("D", D, (H,), dev)
+    _f32_contig("delta_bias", delta_bias, (H,), dev)
+    _f32_contig("h0", h0, (b, H, N, P), dev)
+    y = out if out is not None else torch.empty((b, L, H, P), device=dev, dtype=x.dtype)
+    hl = h_last
+    if hl is None and return_last_state:
+        hl = torch.empty((b, H, N, P), device=dev, dtype=torch.float32)
+    _f32_contig("h_last", hl, (b, H, N, P), dev)
+    p = SSDParams()
+    p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups = b, L, H, P, N, G
+    p.chunk_size, p.io_dtype, p.delta_softplus = int(chunk_size), io, int(bool(delta_softplus))
+    p.x, p.delta, p.A, p.B, p.C, p.D, p.z = _ptr(x), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z)
+    p.delta_bias, p.h0, p.y, p.h_last = _ptr(delta_bias), _ptr(h0), _ptr(y), _ptr(hl)
+    ws_bytes = lib.ssd_chunk_scan_workspace_size(ctypes.byref(p))
+    if ws_bytes == ctypes.c_size_t(-1).value:
+        _check(lib, lib.ssd_chunk_scan_fwd(ctypes.byref(p), None))
+    ws = None
+    if ws_bytes > 0:
+        ws = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+        p.workspace, p.workspace_bytes = _ptr(ws), ws_bytes
+    with torch.cuda.device(dev):
+        _check(lib, lib.ssd_chunk_scan_fwd(ctypes.byref(p), _stream_handle(stream)))
+    return y, hl
+
+
+def ssm_scan_fwd_host(inputs: dict, device="cuda", stream=None, dev_buffers: dict | None = None, **kw):
+    """End-to-end call for host buffers: copy the (pinned) host inputs to the device on the
+    stream, run ssm_scan_fwd, copy y and h_last back into pinned host tensors, synchronise.
+    ``dev_buffers`` may hold reusable device tensors keyed like ``inputs``."""
+    st = stream if stream is not None else torch.cuda.current_stream(device)
+    dev_in = {}
+    with torch.cuda.stream(st):
+        for k, v in inputs.items():
+            if v is None:
+                dev_in[k] = None
+                continue
+            buf = dev_buffers.get(k) if dev_buffers else None
+            if buf is None:
+                buf = torch.empty(v.shape, dtype=v.dtype, device=device)
+                if dev_buffers is not None:
+                    dev_buffers[k] = buf
+            buf.copy_(v, non_blocking=True)
+            dev_in[k] = buf
+        y, hl = ssm_scan_fwd(**dev_in, stream=st, **kw)
+        y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        y_host.copy_(y, non_blocking=True)
+        hl_host = None
+        if hl is not None:
+            hl_host = torch.empty(hl.shape, dtype=hl.dtype, pin_memory=True)
+            hl_host.copy_(hl, non_blocking=True)
+    st.synchronize()
+    return y_host, hl_host
+
+
+def workspace_status(workspace: torch.Tensor | None, stream=None) -> int:
+    """Synchronise the stream and return the device-side status the last call latched."""
+    lib = load_library()
+    return lib.ssm_workspace_status(_ptr(workspace), _stream_handle(stream))

@@ -1,0 +1,272 @@
+// C-ABI entry points of libssmscan.so: host-side validation, path selection and launch.
+// Every argument problem is found here, before anything is enqueued.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "internal.h"
+#include "ssmscan.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+ssm_status_t fail(ssm_status_t s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+ssm_status_t ok() {
+    g_last_error[0] = '\0';
+    return SSM_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// A strided view of `sizes` may not use negative strides.
+bool strides_nonneg(const int64_t* st, int nd) {
+    for (int i = 0; i < nd; ++i)
+        if (st[i] < 0) return false;
+    return true;
+}
+
+// Sufficient condition for a view to have no two index tuples at one address: sorted by
+// stride, each dimension of size > 1 steps over everything the smaller ones span.
+bool non_overlapping(const int64_t* sizes, const int64_t* st, int nd) {
+    int64_t sz[4], sd[4];
+    int k = 0;
+    for (int i = 0; i < nd; ++i)
+        if (sizes[i] > 1) {
+            sz[k] = sizes[i];
+            sd[k] = st[i];
+            ++k;
+        }
+    for (int i = 0; i < k; ++i)
+        for (int j = i + 1; j < k; ++j)
+            if (sd[j] < sd[i]) {
+                std::swap(sd[i], sd[j]);
+                std::swap(sz[i], sz[j]);
+            }
+    int64_t span = 1;
+    for (int i = 0; i < k; ++i) {
+        if (sd[i] < span) return false;
+        span = sd[i] * sz[i];
+    }
+    return true;
+}
+
+constexpr int64_t kMaxDState = 256;
+
+ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
+    if (!p) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1 || p->dim < 1 || p->seqlen < 0)
+        return fail(SSM_ERR_INVALID_ARG, "need batch >= 1, dim >= 1, seqlen >= 0 (got %lld, %lld, %lld)",
+                    (long long)p->batch, (long long)p->dim, (long long)p->seqlen);
+    if (p->dstate < 1) return fail(SSM_ERR_INVALID_ARG, "dstate must be >= 1");
+    if (p->dstate > kMaxDState)
+        return fail(SSM_ERR_UNSUPPORTED, "dstate %lld > %lld", (long long)p->dstate, (long long)kMaxDState);
+    if (p->io_dtype != SSM_DTYPE_F32 && p->io_dtype != SSM_DTYPE_BF16)
+        return fail(SSM_ERR_INVALID_ARG, "io_dtype %d unknown", p->io_dtype);
+    if (p->discretization != SSM_DISC_DELTA_B && p->discretization != SSM_DISC_ZOH)
+        return fail(SSM_ERR_INVALID_ARG, "discretization %d unknown", p->discretization);
+    if ((p->delta_softplus != 0 && p->delta_softplus != 1) || (p->reverse != 0 && p->reverse != 1))
+        return fail(SSM_ERR_INVALID_ARG, "delta_softplus and reverse must be 0 or 1");
+    if (p->chunk_len < 0) return fail(SSM_ERR_INVALID_ARG, "chunk_len must be >= 0");
+    if (!p->A) return fail(SSM_ERR_INVALID_ARG, "A is NULL");
+    if (p->seqlen > 0 && (!p->x || !p->delta || !p->B || !p->C || !p->y))
+        return fail(SSM_ERR_INVALID_ARG, "x, delta, B, C and y are required");
+    const size_t esz = p->io_dtype == SSM_DTYPE_BF16 ? 2 : 4;
+    const void* io[] = {p->x, p->delta, p->B, p->C, p->z, p->y};
+    for (const void* q : io)
+        if (q && !aligned(q, esz)) return fail(SSM_ERR_INVALID_ARG, "I/O pointer not aligned to its dtype");
+    const void* f32[] = {p->A, p->D, p->delta_bias, p->h0, p->h_last};
+    for (const void* q : f32)
+        if (q && !aligned(q, 4)) return fail(SSM_ERR_INVALID_ARG, "fp32 pointer not 4-byte aligned");
+    const int64_t* strides[] = {p->x_stride, p->delta_stride, p->z_stride, p->y_stride, p->B_stride, p->C_stride};
+    for (const int64_t* s : strides)
+        if (!strides_nonneg(s, 3)) return fail(SSM_ERR_INVALID_ARG, "negative stride");
+    const int64_t ysz[3] = {p->batch, p->seqlen, p->dim};
+    if (p->seqlen > 0 && !non_overlapping(ysz, p->y_stride, 3))
+        return fail(SSM_ERR_INVALID_ARG, "y strides overlap");
+    if (p->h_last && p->h0 && p->h_last != p->h0) {
+        const char* a0 = reinterpret_cast<const char*>(p->h0);
+        const char* a1 = reinterpret_cast<const char*>(p->h_last);
+        const int64_t bytes = p->batch * p->dim * p->dstate * 4;
+        if (a1 < a0 + bytes && a0 < a1 + bytes) return fail(SSM_ERR_INVALID_ARG, "h0 and h_last partly overlap");
+    }
+    ssm::ScanArgs& a = *out;
+    a.batch = p->batch;
+    a.seqlen = p->seqlen;
+    a.dim = p->dim;
+    a.dstate = (int)p->dstate;
+    a.io_bf16 = p->io_dtype == SSM_DTYPE_BF16;
+    a.softplus = p->delta_softplus;
+    a.reverse = p->reverse;
+    a.zoh = p->discretization == SSM_DISC_ZOH;
+    a.x = p->x;
+    a.delta = p->delta;
+    a.B = p->B;
+    a.C = p->C;
+    a.z = p->z;
+    a.A = p->A;
+    a.D = p->D;
+    a.bias = p->delta_bias;
+    a.h0 = p->h0;
+    a.y = p->y;
+    a.h_last = p->h_last;
+    for (int i = 0; i < 3; ++i) {
+        a.xs[i] = p->x_stride[i];
+        a.ds[i] = p->delta_stride[i];
+        a.zs[i] = p->z_stride[i];
+        a.ys[i] = p->y_stride[i];
+        a.Bs[i] = p->B_stride[i];
+        a.Cs[i] = p->C_stride[i];
+    }
+    a.chunk_len = p->chunk_len;
+    a.workspace = p->workspace;
+    a.workspace_bytes = p->workspace_bytes;
+    return SSM_OK;
+}
+
+size_t scan_workspace_bytes(const ssm::ScanArgs&) { return 0; }
+
+ssm_status_t cuda_fail(cudaError_t e) {
+    return fail(SSM_ERR_CUDA, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+ssm_status_t validate_ssd(const ssd_scan_params* p, ssm::SSDArgs* out) {
+    if (!p) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1 || p->seqlen < 0 || p->nheads < 1 || p->headdim < 1 || p->dstate < 1 || p->ngroups < 1)
+        return fail(SSM_ERR_INVALID_ARG, "need batch, nheads, headdim, dstate, ngroups >= 1 and seqlen >= 0");
+    if (p->nheads % p->ngroups != 0) return fail(SSM_ERR_INVALID_ARG, "ngroups must divide nheads");
+    if (p->chunk_size < 1) return fail(SSM_ERR_INVALID_ARG, "chunk_size must be >= 1");
+    if (p->io_dtype != SSM_DTYPE_F32 && p->io_dtype != SSM_DTYPE_BF16)
+        return fail(SSM_ERR_INVALID_ARG, "io_dtype %d unknown", p->io_dtype);
+    if (p->delta_softplus != 0 && p->delta_softplus != 1)
+        return fail(SSM_ERR_INVALID_ARG, "delta_softplus must be 0 or 1");
+    if (!p->A) return fail(SSM_ERR_INVALID_ARG, "A is NULL");
+    if (p->seqlen > 0 && (!p->x || !p->delta || !p->B || !p->C || !p->y))
+        return fail(SSM_ERR_INVALID_ARG, "x, delta, B, C and y are required");
+    if (p->headdim > 256 || p->dstate > 256)
+        return fail(SSM_ERR_UNSUPPORTED, "headdim and dstate must be <= 256");
+    const int64_t J = 256 / p->headdim;
+    if ((p->dstate + J - 1) / J > 64)
+        return fail(SSM_ERR_UNSUPPORTED, "dstate %lld too large for headdim %lld", (long long)p->dstate,
+                    (long long)p->headdim);
+    const size_t esz = p->io_dtype == SSM_DTYPE_BF16 ? 2 : 4;
+    const void* io[] = {p->x, p->delta, p->B, p->C, p->z, p->y};
+    for (const void* q : io)
+        if (q && !aligned(q, esz)) return fail(SSM_ERR_INVALID_ARG, "I/O pointer not aligned to its dtype");
+    const void* f32[] = {p->A, p->D, p->delta_bias, p->h0, p->h_last};
+    for (const void* q : f32)
+        if (q && !aligned(q, 4)) return fail(SSM_ERR_INVALID_ARG, "fp32 pointer not 4-byte aligned");
+    ssm::SSDArgs& a = *out;
+    a.batch = p->batch;
+    a.seqlen = p->seqlen;
+    a.nheads = p->nheads;
+    a.headdim = p->headdim;
+    a.dstate = p->dstate;
+    a.ngroups = p->ngroups;
+    a.chunk = p->chunk_size;
+    a.io_bf16 = p->io_dtype == SSM_DTYPE_BF16;
+    a.softplus = p->delta_softplus;
+    a.x = p->x;
+    a.delta = p->delta;
+    a.A = p->A;
+    a.B = p->B;
+    a.C = p->C;
+    a.D = p->D;
+    a.z = p->z;
+    a.bias = p->delta_bias;
+    a.h0 = p->h0;
+    a.y = p->y;
+    a.h_last = p->h_last;
+    a.workspace = p->workspace;
+    a.workspace_bytes = p->workspace_bytes;
+    return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_scan_workspace_size(const ssm_scan_params* p) {
+    ssm::ScanArgs a;
+    if (validate_scan(p, &a) != SSM_OK) return (size_t)-1;
+    return scan_workspace_bytes(a);
+}
+
+ssm_status_t ssm_scan_fwd(const ssm_scan_params* p, void* stream) {
+    ssm::ScanArgs a;
+    ssm_status_t s = validate_scan(p, &a);
+    if (s != SSM_OK) return s;
+    const size_t need = scan_workspace_bytes(a);
+    if (need > 0 && (!a.workspace || a.workspace_bytes < need || !aligned(a.workspace, 256)))
+        return fail(SSM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (a.seqlen == 0) {
+        if (a.h_last) {
+            const size_t bytes = (size_t)(a.batch * a.dim * a.dstate) * sizeof(float);
+            e = a.h0 ? (a.h0 == a.h_last ? cudaSuccess
+                                         : cudaMemcpyAsync(a.h_last, a.h0, bytes, cudaMemcpyDeviceToDevice, st))
+                     : cudaMemsetAsync(a.h_last, 0, bytes, st);
+        }
+    } else {
+        e = ssm::launch_scan_generic(a, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ok();
+}
+
+size_t ssd_chunk_scan_workspace_size(const ssd_scan_params* p) {
+    ssm::SSDArgs a;
+    if (validate_ssd(p, &a) != SSM_OK) return (size_t)-1;
+    return 0;
+}
+
+ssm_status_t ssd_chunk_scan_fwd(const ssd_scan_params* p, void* stream) {
+    ssm::SSDArgs a;
+    ssm_status_t s = validate_ssd(p, &a);
+    if (s != SSM_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = ssm::launch_ssd_reference(a, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ok();
+}
+
+ssm_status_t ssm_workspace_status(const void* workspace, void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (!workspace) return ok();
+    uint32_t word = 0;
+    e = cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (word != 0) return fail(SSM_ERR_TIMEOUT, "device status word %u", word);
+    return ok();
+}
+
+const char* ssm_status_string(ssm_status_t s) {
+    switch (s) {
+        case SSM_OK: return "SSM_OK";
+        case SSM_ERR_INVALID_ARG: return "SSM_ERR_INVALID_ARG";
+        case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED";
+        case SSM_ERR_CUDA: return "SSM_ERR_CUDA";
+        case SSM_ERR_TIMEOUT: return "SSM_ERR_TIMEOUT";
+        case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE";
+    }
+    return "SSM_ERR_UNKNOWN";
+}
+
+const char* ssm_last_error(void) { return g_last_error; }
+
+int ssm_abi_version(void) { return SSMSCAN_ABI_VERSION; }
+
+}  // extern "C"

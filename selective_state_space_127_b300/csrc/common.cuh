@@ -1,0 +1,54 @@
+// Device helpers shared by the kernels: dtype conversion and fast transcendental forms.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace ssm {
+
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
+constexpr float kLn2 = 0.6931471805599453f;    // ln(2)
+
+__device__ __forceinline__ float load_f32(const void* p, int64_t i, int bf16) {
+    return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i])
+                : static_cast<const float*>(p)[i];
+}
+
+__device__ __forceinline__ void store_io(void* p, int64_t i, float v, int bf16) {
+    if (bf16)
+        static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+    else
+        static_cast<float*>(p)[i] = v;
+}
+
+// 2^x with the SFU (ex2.approx.ftz.f32: relative error about 2^-22, flushes denormals).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// log2(x) with the SFU.
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// 1/x with the SFU.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// softplus(v) = log(1 + e^v) through CUDA's accurate expf/log1pf; v > 20 returns v
+// (log1p(e^-v) < 2.1e-9 is below fp32 resolution there).
+__device__ __forceinline__ float softplus_accurate(float v) {
+    return v > 20.f ? v : log1pf(expf(v));
+}
+
+// silu(z) = z / (1 + e^-z) through CUDA's accurate expf and an IEEE division.
+__device__ __forceinline__ float silu_accurate(float z) { return z / (1.f + expf(-z)); }
+
+}  // namespace ssm

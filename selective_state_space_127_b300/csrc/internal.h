@@ -1,0 +1,60 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ssmscan.h"
+
+namespace ssm {
+
+// Host-validated selective-scan arguments, passed to kernels by value.
+struct ScanArgs {
+    int64_t batch, seqlen, dim;
+    int dstate;
+    int io_bf16;
+    int softplus, reverse, zoh;
+    const void* x;
+    const void* delta;
+    const void* B;
+    const void* C;
+    const void* z;
+    const float* A;
+    const float* D;
+    const float* bias;
+    const float* h0;
+    void* y;
+    float* h_last;
+    int64_t xs[3], ds[3], zs[3], ys[3], Bs[3], Cs[3];
+    int64_t chunk_len;
+    void* workspace;
+    size_t workspace_bytes;
+};
+
+struct SSDArgs {
+    int64_t batch, seqlen, nheads, headdim, dstate, ngroups, chunk;
+    int io_bf16;
+    int softplus;
+    const void* x;
+    const void* delta;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* bias;
+    const float* h0;
+    void* y;
+    float* h_last;
+    void* workspace;
+    size_t workspace_bytes;
+};
+
+// Which selective-scan kernel a call takes.
+enum class ScanPath { Generic = 0, Fast = 1, ChunkCarry = 2 };
+
+// Kernel launchers: return cudaSuccess or the launch error. They assume valid args.
+cudaError_t launch_scan_generic(const ScanArgs& a, cudaStream_t s);
+cudaError_t launch_ssd_reference(const SSDArgs& a, cudaStream_t s);
+
+}  // namespace ssm

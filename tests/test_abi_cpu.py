@@ -1,0 +1,141 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from selective_state_space_127_b300 import binding
+from selective_state_space_127_b300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssmscan.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return binding.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SSMSCAN_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.check_output(["nm", "-D", "--defined-only", binding.LIB_PATH]).decode()
+    exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
+    missing = [f for f in _declared_functions() if f not in exported]
+    assert not missing, missing
+    for f in _declared_functions():
+        assert hasattr(lib, f)
+
+
+def test_library_needs_no_cuda_shared_runtime():
+    out = subprocess.check_output(["ldd", binding.LIB_PATH]).decode()
+    assert "libcudart" not in out and "libtorch" not in out
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.ssm_abi_version() == binding.ABI_VERSION
+    for code in range(6):
+        assert lib.ssm_status_string(code).decode() == binding._status_name(code)
+
+
+def _c_offsets(struct, fields):
+    src = "#include <stdio.h>\n#include <stddef.h>\n#include \"ssmscan.h\"\nint main(void){\n"
+    for f in fields:
+        src += f'printf("%zu\\n", offsetof({struct}, {f}));\n'
+    src += f'printf("%zu\\n", sizeof({struct}));\nreturn 0;}}\n'
+    return src
+
+
+@pytest.mark.parametrize("struct,cls", [("ssm_scan_params", binding.ScanParams),
+                                        ("ssd_scan_params", binding.SSDParams)])
+def test_ctypes_struct_layout_matches_header(tmp_path, struct, cls):
+    fields = [f for f, _ in cls._fields_]
+    c = tmp_path / "probe.c"
+    c.write_text(_c_offsets(struct, fields))
+    exe = tmp_path / "probe"
+    subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), str(c), "-o", str(exe)])
+    vals = [int(v) for v in subprocess.check_output([str(exe)]).decode().split()]
+    assert vals[:-1] == [getattr(cls, f).offset for f in fields]
+    assert vals[-1] == ctypes.sizeof(cls)
+
+
+def _valid_scan_params():
+    p = binding.ScanParams()
+    p.batch, p.seqlen, p.dim, p.dstate = 2, 8, 4, 16
+    p.io_dtype = binding.SSM_DTYPE_BF16
+    p.delta_softplus = 1
+    fake = 1 << 20  # an aligned, never-dereferenced address: validation only
+    for name in ("x", "delta", "B", "C", "A", "y"):
+        setattr(p, name, fake)
+    p.x_stride[:] = (32, 4, 1)
+    p.delta_stride[:] = (32, 4, 1)
+    p.y_stride[:] = (32, 4, 1)
+    p.B_stride[:] = (128, 16, 1)
+    p.C_stride[:] = (128, 16, 1)
+    return p
+
+
+def test_workspace_query_accepts_valid_params(lib):
+    p = _valid_scan_params()
+    assert lib.ssm_scan_workspace_size(ctypes.byref(p)) != ctypes.c_size_t(-1).value
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("batch", 0, binding.SSM_ERR_INVALID_ARG),
+    ("dim", -1, binding.SSM_ERR_INVALID_ARG),
+    ("seqlen", -5, binding.SSM_ERR_INVALID_ARG),
+    ("dstate", 0, binding.SSM_ERR_INVALID_ARG),
+    ("dstate", 257, binding.SSM_ERR_UNSUPPORTED),
+    ("io_dtype", 7, binding.SSM_ERR_INVALID_ARG),
+    ("discretization", 3, binding.SSM_ERR_INVALID_ARG),
+    ("reverse", 2, binding.SSM_ERR_INVALID_ARG),
+    ("A", 0, binding.SSM_ERR_INVALID_ARG),
+    ("x", 0, binding.SSM_ERR_INVALID_ARG),
+    ("y", (1 << 20) + 1, binding.SSM_ERR_INVALID_ARG),
+    ("chunk_len", -1, binding.SSM_ERR_INVALID_ARG),
+])
+def test_invalid_scan_args_are_rejected_before_launch(lib, field, value, status):
+    p = _valid_scan_params()
+    setattr(p, field, value)
+    assert lib.ssm_scan_workspace_size(ctypes.byref(p)) == ctypes.c_size_t(-1).value
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == status
+    assert lib.ssm_last_error().decode() != ""
+
+
+def test_overlapping_output_strides_are_rejected(lib):
+    p = _valid_scan_params()
+    p.y_stride[:] = (32, 1, 1)   # t and d step onto the same elements
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
+    p = _valid_scan_params()
+    p.x_stride[:] = (32, -4, 1)
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
+
+
+def test_invalid_ssd_args_are_rejected_before_launch(lib):
+    p = binding.SSDParams()
+    p.batch, p.seqlen, p.nheads, p.headdim, p.dstate, p.ngroups, p.chunk_size = 1, 16, 6, 8, 16, 4, 8
+    fake = 1 << 20
+    for name in ("x", "delta", "A", "B", "C", "y"):
+        setattr(p, name, fake)
+    p.io_dtype, p.delta_softplus = binding.SSM_DTYPE_BF16, 1
+    assert lib.ssd_chunk_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG   # 4 does not divide 6
+    p.ngroups = 2
+    p.chunk_size = 0
+    assert lib.ssd_chunk_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
+    p.chunk_size = 8
+    assert lib.ssd_chunk_scan_workspace_size(ctypes.byref(p)) != ctypes.c_size_t(-1).value
+
+
+def test_null_params_are_rejected(lib):
+    assert lib.ssm_scan_fwd(None, None) == binding.SSM_ERR_INVALID_ARG
+    assert lib.ssd_chunk_scan_fwd(None, None) == binding.SSM_ERR_INVALID_ARG

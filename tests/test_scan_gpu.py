@@ -1,0 +1,193 @@
+"""GPU parity of the selective scan (through the C ABI) against the fp64 oracle.
+
+Tolerances: rel-L2 over the compared tensor, <= 1e-5 for fp32 I/O and <= 2e-2 for bf16 I/O
+(the state is fp32 either way; h_last is fp32 and held to 1e-4 for bf16 inputs, because the
+oracle sees the same bf16-rounded inputs and only fp32 arithmetic separates the two).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from selective_state_space_127_b300 import binding, ssm_scan_fwd
+from selective_state_space_127_b300.synth import SCAN_WORKLOADS, make_scan_inputs, scan_workload_inputs
+from conftest import rel_l2
+
+pytestmark = pytest.mark.gpu
+
+TOL_Y = {"f32": 1e-5, "bf16": 2e-2}
+TOL_H = {"f32": 1e-5, "bf16": 1e-4}
+
+
+def _to(dev, inp):
+    return {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+
+
+def _run_both(inp, dev, **kw):
+    g = _to(dev, inp)
+    y, h = ssm_scan_fwd(**g, **kw)
+    torch.cuda.synchronize()
+    okw = {k: v for k, v in kw.items() if k in ("delta_softplus", "h0", "zoh", "reverse")}
+    if "h0" in okw and okw["h0"] is not None:
+        okw["h0"] = okw["h0"].cpu()
+    y_ref, h_ref = oracle.ssm_scan_ref(**inp, **okw)
+    return y.float().cpu().numpy(), h.cpu().numpy(), y_ref, h_ref
+
+
+def test_tiny_fp32_workload_matches_oracle(cuda_dev):
+    inp = scan_workload_inputs(0)
+    y, h, y_ref, h_ref = _run_both(inp, cuda_dev)
+    assert rel_l2(y, y_ref) <= TOL_Y["f32"]
+    assert rel_l2(h, h_ref) <= TOL_H["f32"]
+
+
+CASES = [
+    # b, L, D, N, dtype, gate, dskip
+    (1, 1, 1, 1, "f32", True, True),
+    (2, 7, 5, 3, "f32", False, False),
+    (3, 64, 33, 16, "f32", True, True),
+    (2, 200, 130, 16, "bf16", True, True),
+    (1, 129, 70, 8, "bf16", False, True),
+    (2, 50, 40, 32, "f32", True, False),
+    (1, 90, 17, 64, "f32", True, True),
+    (1, 40, 9, 128, "bf16", True, True),
+    (1, 33, 5, 256, "f32", False, False),
+    (2, 300, 257, 17, "bf16", True, True),
+]
+
+
+@pytest.mark.parametrize("b,L,D,N,dt,gate,dskip", CASES)
+def test_random_shapes_match_oracle(cuda_dev, b, L, D, N, dt, gate, dskip):
+    inp = make_scan_inputs(b, L, D, N, dt, seed=1000 + b * 7 + L + D + N, d_skip="normal" if dskip else "none",
+                           gate=gate)
+    y, h, y_ref, h_ref = _run_both(inp, cuda_dev)
+    assert rel_l2(y, y_ref) <= TOL_Y[dt]
+    assert rel_l2(h, h_ref) <= TOL_H[dt]
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_reverse_zoh_h0_and_no_softplus(cuda_dev, dt):
+    inp = make_scan_inputs(2, 77, 24, 16, dt, seed=77)
+    h0 = torch.randn(2, 24, 16, generator=torch.Generator().manual_seed(3))
+    for kw in (dict(reverse=True), dict(zoh=True), dict(h0=h0), dict(delta_softplus=False),
+               dict(reverse=True, zoh=True, h0=h0)):
+        kw2 = dict(kw)
+        if "h0" in kw2:
+            kw2["h0"] = kw2["h0"].to(cuda_dev)
+        g = _to(cuda_dev, inp)
+        if not kw.get("delta_softplus", True):
+            # without softplus the step is delta + bias itself: keep it positive
+            g["delta"] = g["delta"].abs() * 0.05
+            g["delta_bias"] = torch.full_like(g["delta_bias"], 1e-3)
+            ref_in = dict(inp, delta=g["delta"].cpu(), delta_bias=g["delta_bias"].cpu())
+        else:
+            ref_in = inp
+        y, h = ssm_scan_fwd(**g, **kw2)
+        y_ref, h_ref = oracle.ssm_scan_ref(**ref_in, **kw)
+        assert rel_l2(y.float().cpu().numpy(), y_ref) <= TOL_Y[dt], kw
+        assert rel_l2(h.cpu().numpy(), h_ref) <= TOL_H[dt], kw
+
+
+def test_strided_views_like_the_mamba_block(cuda_dev):
+    """x and z as the two halves of one in_proj output (b, L, 2D); delta with one value per
+    token broadcast over channels (channel stride 0); y written into a strided slice."""
+    g = torch.Generator().manual_seed(5)
+    b, L, D, N = 2, 96, 40, 16
+    xz = torch.randn(b, L, 2 * D, generator=g).to(torch.bfloat16)
+    delta_tok = torch.randn(b, L, 1, generator=g).to(torch.bfloat16)
+    B = torch.randn(b, L, N, generator=g).to(torch.bfloat16)
+    C = torch.randn(b, L, N, generator=g).to(torch.bfloat16)
+    A = -torch.arange(1, N + 1, dtype=torch.float32).repeat(D, 1)
+    Dv = torch.randn(D, generator=g)
+    bias = torch.full((D,), -3.0)
+    dev = cuda_dev
+    xz_d = xz.to(dev)
+    x_d, z_d = xz_d[..., :D], xz_d[..., D:]
+    delta_d = delta_tok.to(dev).expand(b, L, D)
+    assert delta_d.stride(2) == 0
+    out_big = torch.zeros(b, L, 3 * D, dtype=torch.bfloat16, device=dev)
+    y_view = out_big[..., D:2 * D]
+    BC = torch.stack([B, C], dim=2).to(dev)   # (b, L, 2, N): B and C interleaved rows
+    y, h = ssm_scan_fwd(x_d, delta_d, A.to(dev), BC[:, :, 0], BC[:, :, 1], Dv.to(dev), z_d, bias.to(dev), out=y_view)
+    torch.cuda.synchronize()
+    y_ref, h_ref = oracle.ssm_scan_ref(xz[..., :D], delta_tok.expand(b, L, D), A, B, C, Dv, xz[..., D:], bias)
+    assert rel_l2(out_big[..., D:2 * D].float().cpu().numpy(), y_ref) <= TOL_Y["bf16"]
+    assert torch.all(out_big[..., :D] == 0) and torch.all(out_big[..., 2 * D:] == 0)
+    assert rel_l2(h.cpu().numpy(), h_ref) <= TOL_H["bf16"]
+
+
+def test_channel_major_input_layout(cuda_dev):
+    """x stored (b, D, L) and passed as its (b, L, D) transpose view."""
+    inp = make_scan_inputs(2, 70, 12, 16, "f32", seed=8)
+    g = _to(cuda_dev, inp)
+    g["x"] = g["x"].transpose(1, 2).contiguous().transpose(1, 2)
+    g["z"] = g["z"].transpose(1, 2).contiguous().transpose(1, 2)
+    assert g["x"].stride(1) == 1
+    y, h = ssm_scan_fwd(**g)
+    y_ref, h_ref = oracle.ssm_scan_ref(**inp)
+    assert rel_l2(y.cpu().numpy(), y_ref) <= TOL_Y["f32"]
+
+
+def test_empty_sequence_copies_h0(cuda_dev):
+    inp = make_scan_inputs(2, 0, 6, 4, "f32", seed=9)
+    g = _to(cuda_dev, inp)
+    h0 = torch.randn(2, 6, 4, device=cuda_dev)
+    y, h = ssm_scan_fwd(**g, h0=h0)
+    torch.cuda.synchronize()
+    assert y.shape == (2, 0, 6)
+    assert torch.equal(h, h0)
+    y, h = ssm_scan_fwd(**g)
+    torch.cuda.synchronize()
+    assert torch.all(h == 0)
+
+
+def test_split_and_resume_on_gpu(cuda_dev):
+    inp = make_scan_inputs(2, 300, 64, 16, "f32", seed=10)
+    g = _to(cuda_dev, inp)
+    y, h = ssm_scan_fwd(**g)
+    cut = 113
+    first = {k: (v[:, :cut] if k in ("x", "delta", "B", "C", "z") else v) for k, v in g.items()}
+    second = {k: (v[:, cut:] if k in ("x", "delta", "B", "C", "z") else v) for k, v in g.items()}
+    y1, h1 = ssm_scan_fwd(**first)
+    y2, h2 = ssm_scan_fwd(**second, h0=h1)
+    torch.cuda.synchronize()
+    assert rel_l2(torch.cat([y1, y2], 1).cpu().numpy(), y.cpu().numpy()) <= 1e-6
+    assert rel_l2(h2.cpu().numpy(), h.cpu().numpy()) <= 1e-6
+
+
+def _sampled_parity(k, dev, n_chan=48, seed=0):
+    w = SCAN_WORKLOADS[k]
+    inp = scan_workload_inputs(k, device=dev)
+    y, h = ssm_scan_fwd(**inp, chunk_len=w.chunk_len)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(seed)
+    idx = torch.tensor(np.sort(rng.choice(w.dim, size=min(n_chan, w.dim), replace=False)), device=dev)
+    sub = {k2: (v.index_select(2, idx) if k2 in ("x", "delta", "z") else v) for k2, v in inp.items()}
+    sub["A"] = inp["A"].index_select(0, idx)
+    sub["D"] = inp["D"].index_select(0, idx) if inp["D"] is not None else None
+    sub["delta_bias"] = inp["delta_bias"].index_select(0, idx)
+    y_ref, h_ref = oracle.ssm_scan_ref(**{k2: (v.cpu() if v is not None else None) for k2, v in sub.items()})
+    y_s = y.index_select(2, idx).float().cpu().numpy()
+    h_s = h.index_select(1, idx).cpu().numpy()
+    return rel_l2(y_s, y_ref), rel_l2(h_s, h_ref)
+
+
+@pytest.mark.parametrize("k", [1, 2, 3])
+def test_full_size_workloads_on_sampled_channels(cuda_dev, k):
+    ey, eh = _sampled_parity(k, cuda_dev, n_chan=32 if k == 3 else 64, seed=k)
+    print(f"workload {k}: rel-L2 y {ey:.3e}  h_last {eh:.3e}")
+    assert ey <= TOL_Y["bf16"]
+    assert eh <= TOL_H["bf16"]
+
+
+def test_invalid_args_raise_without_launch(cuda_dev):
+    inp = _to(cuda_dev, make_scan_inputs(1, 8, 4, 4, "f32", seed=1))
+    with pytest.raises(ValueError):
+        ssm_scan_fwd(**dict(inp, B=inp["B"].to(torch.bfloat16)))
+    inp2 = dict(inp)
+    inp2["A"] = torch.zeros(4, 300, device=cuda_dev)
+    inp2["B"] = torch.zeros(1, 8, 300, device=cuda_dev)
+    inp2["C"] = torch.zeros(1, 8, 300, device=cuda_dev)
+    with pytest.raises(binding.SSMError) as e:
+        ssm_scan_fwd(**inp2)
+    assert e.value.status == binding.SSM_ERR_UNSUPPORTED

@@ -1,0 +1,75 @@
+"""GPU parity of the SSD chunked scan (through the C ABI) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from selective_state_space_127_b300 import ssd_chunk_scan_fwd
+from selective_state_space_127_b300.synth import SSD_WORKLOAD, make_ssd_inputs, ssd_workload_inputs
+from conftest import rel_l2
+
+pytestmark = pytest.mark.gpu
+
+TOL_Y = {"f32": 1e-5, "bf16": 2e-2}
+TOL_H = {"f32": 1e-5, "bf16": 1e-4}
+
+
+def _to(dev, inp):
+    return {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+
+
+CASES = [
+    # b, L, H, P, N, G, Q, dtype, gate, dskip
+    (1, 1, 1, 1, 1, 1, 1, "f32", False, False),
+    (2, 37, 3, 8, 16, 1, 16, "f32", True, True),
+    (1, 300, 4, 64, 128, 1, 256, "bf16", False, False),
+    (2, 100, 4, 32, 64, 2, 64, "bf16", True, True),
+    (1, 513, 2, 64, 128, 1, 256, "bf16", False, False),
+    (1, 64, 2, 16, 32, 1, 32, "f32", False, True),
+]
+
+
+@pytest.mark.parametrize("b,L,H,P,N,G,Q,dt,gate,dskip", CASES)
+def test_random_shapes_match_oracle(cuda_dev, b, L, H, P, N, G, Q, dt, gate, dskip):
+    inp = make_ssd_inputs(b, L, H, P, N, dt, seed=500 + L + H + P + N, d_skip="normal" if dskip else "none",
+                          gate=gate, ngroups=G)
+    y, h = ssd_chunk_scan_fwd(**_to(cuda_dev, inp), chunk_size=Q)
+    torch.cuda.synchronize()
+    y_ref, h_ref = oracle.ssd_scan_ref(**inp)
+    assert rel_l2(y.float().cpu().numpy(), y_ref) <= TOL_Y[dt]
+    assert rel_l2(h.cpu().numpy(), h_ref) <= TOL_H[dt]
+
+
+def test_h0_and_chunk_size_invariance(cuda_dev):
+    inp = make_ssd_inputs(1, 200, 2, 64, 128, "bf16", seed=77)
+    h0 = torch.randn(1, 2, 128, 64, generator=torch.Generator().manual_seed(1))
+    g = _to(cuda_dev, inp)
+    outs = []
+    for Q in (32, 64, 128, 256):
+        y, h = ssd_chunk_scan_fwd(**g, chunk_size=Q, h0=h0.to(cuda_dev))
+        outs.append((y.float().cpu().numpy(), h.cpu().numpy()))
+    y_ref, h_ref = oracle.ssd_scan_ref(**inp, h0=h0)
+    for y, h in outs:
+        assert rel_l2(y, y_ref) <= TOL_Y["bf16"]
+        assert rel_l2(h, h_ref) <= TOL_H["bf16"]
+        assert rel_l2(y, outs[0][0]) <= 1e-2
+
+
+def test_full_size_workload_on_sampled_heads(cuda_dev):
+    w = SSD_WORKLOAD
+    inp = ssd_workload_inputs(device=cuda_dev)
+    y, h = ssd_chunk_scan_fwd(**inp, chunk_size=w.chunk)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(4)
+    heads = torch.tensor(np.sort(rng.choice(w.nheads, size=6, replace=False)), device=cuda_dev)
+    sub = dict(inp)
+    sub["x"] = inp["x"].index_select(2, heads)
+    sub["delta"] = inp["delta"].index_select(2, heads)
+    sub["A"] = inp["A"].index_select(0, heads)
+    sub["delta_bias"] = inp["delta_bias"].index_select(0, heads)
+    y_ref, h_ref = oracle.ssd_scan_ref(**{k: (v.cpu() if v is not None else None) for k, v in sub.items()})
+    ey = rel_l2(y.index_select(2, heads).float().cpu().numpy(), y_ref)
+    eh = rel_l2(h.index_select(1, heads).cpu().numpy(), h_ref)
+    print(f"SSD workload: rel-L2 y {ey:.3e}  h_last {eh:.3e}")
+    assert ey <= TOL_Y["bf16"]
+    assert eh <= TOL_H["bf16"]
