@@ -1,0 +1,417 @@
+#!/usr/bin/env python
+"""Benchmark of the selective-scan hot path on B300, one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one selective scan (softplus, discretisation, recurrence, C readout, D skip,
+silu gate, final state) over the Mamba-130M-shaped layer workload b=8, D=1536, L=2048,
+N=16, bf16 I/O, fp32 state, with inputs resident in HBM. ``value`` is GB/s of algorithmic
+bytes (every input read once, every output written once) over all ranks; the SSD chunked
+scan (b=4, H=64, P=64, N=128, L=4096, Q=256) is timed the same way and reported in
+``ssd`` as TFLOP/s. Under torchrun each rank runs its own replica (different seed): the
+path shards with no collective, so scaling is weak.
+
+``--impl reference`` times the fp64 CPU oracle instead, on bounded samples of the same
+workload (rank 0 only), and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan GB/s and fraction of B300 HBM peak; SSD TFLOP/s (1 GPU)"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "sm_max_mhz": 2032.0}
+SMS = 148
+# Per-SM, per-clock rates measured on this B300 with a microbenchmark: ex2.approx.f32 at 32
+# per clock per SM, FP32 FMA lanes at 128 per clock per SM. A delta*B state update needs one
+# ex2 and four FP32 operations, so both pipes cap it at 32 updates per clock per SM.
+UPDATES_PER_CLK_SM = 32.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=1, choices=[1, 2, 3])
+    ap.add_argument("--no-ssd", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra-workloads", action="store_true", help="also time scan workloads 2 and 3")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ work accounting
+
+def scan_bytes(w, batch=None, dim=None, seqlen=None):
+    """Algorithmic bytes of one selective scan: x, delta, z read and y written once in the
+    I/O dtype; B, C read once; A, D, bias read once (fp32); h_last written once (fp32)."""
+    b, d, L, n = batch or w.batch, dim or w.dim, seqlen or w.seqlen, w.dstate
+    io = 2 if w.dtype == "bf16" else 4
+    per_bld = (3 + (1 if w.gate else 0)) * io       # x, delta, (z) in, y out
+    tot = b * L * d * per_bld + 2 * b * L * n * io
+    tot += d * n * 4 + d * 4 * (2 if w.d_skip != "none" else 1) + b * d * n * 4
+    return tot
+
+
+def ssd_bytes(w):
+    io = 2
+    return (2 * w.batch * w.seqlen * w.nheads * w.headdim * io + w.batch * w.seqlen * w.nheads * io
+            + 2 * w.batch * w.seqlen * w.dstate * io + 2 * w.nheads * 4
+            + w.batch * w.nheads * w.dstate * w.headdim * 4)
+
+
+def ssd_flops(w):
+    """Useful flops of the chunked SSD algorithm: C B^T (causal half, once per batch and
+    chunk since B and C are head-shared), masked-block times X (causal half), C times the
+    carried state, and the chunk-state update B^T X."""
+    nch = (w.seqlen + w.chunk - 1) // w.chunk
+    Q, N, P = w.chunk, w.dstate, w.headdim
+    cb = w.batch * nch * Q * Q * N                 # 2 * Q*Q/2 * N
+    diag = w.batch * w.nheads * nch * Q * Q * P    # 2 * Q*Q/2 * P
+    off = w.batch * w.nheads * nch * 2 * Q * N * P
+    state = w.batch * w.nheads * nch * 2 * Q * N * P
+    return cb + diag + off + state
+
+
+# ------------------------------------------------------------------ clocks during the timed region
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons with `nvidia-smi -lms 100` (read-only) while the
+    benchmark runs; summary() reports the samples taken inside the marked timed window (or,
+    if the window was shorter than the sampling period, those of the whole loaded phase)."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        import subprocess
+        import torch
+        self.rows = []
+        self.window = None
+        self.err = None
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", uuid, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception as e:  # reported in the JSON line
+            self.proc, self.err = None, str(e)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 7:
+                self.rows.append((time.time(), parts))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=5)
+
+    def summary(self):
+        if self.proc is None:
+            return {"error": self.err}
+        rows = self.rows
+        in_window = False
+        if self.window:
+            inside = [r for r in rows if self.window[0] - 0.05 <= r[0] <= self.window[1] + 0.05]
+            if inside:
+                rows, in_window = inside, True
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        mhz = [num(r[1][0]) for r in rows if num(r[1][0]) is not None]
+        mx = [num(r[1][1]) for r in rows if num(r[1][1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[1][3 + i].lower().startswith("active")})
+        watts = [num(r[1][2]) for r in rows if num(r[1][2]) is not None]
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(watts) if watts else None, "samples": len(rows), "in_window": in_window,
+                "reasons": reasons}
+
+
+# ------------------------------------------------------------------ oracle timing (CPU)
+
+def _oracle_sample(w, target_s):
+    """Pick a sample (batch rows, channels) of workload w that the oracle finishes in about
+    target_s seconds on this host, from a probe of one channel per thread."""
+    import oracle
+    from selective_state_space_127_b300.synth import make_scan_inputs, SEED_BASE
+
+    threads = oracle.max_threads()
+    probe_d = max(1, min(w.dim, threads))
+    inp = make_scan_inputs(1, w.seqlen, probe_d, w.dstate, w.dtype, SEED_BASE + 1, "cpu", w.d_skip, w.gate)
+    conv = {k: (oracle.f64(v) if v is not None else None) for k, v in inp.items()}
+    t0 = time.perf_counter()
+    oracle.ssm_scan_ref(**conv, nthreads=threads)
+    probe_s = max(time.perf_counter() - t0, 1e-6)
+    chans = max(probe_d, int(probe_d * target_s / probe_s))     # channel-sequences that fit
+    rows = max(1, min(w.batch, chans // w.dim))
+    d = w.dim if rows > 1 or chans >= w.dim else max(1, chans)
+    return rows, d, threads
+
+
+def _oracle_inputs(w, rows, d):
+    import oracle
+    from selective_state_space_127_b300.synth import make_scan_inputs, SEED_BASE
+
+    inp = make_scan_inputs(rows, w.seqlen, d, w.dstate, w.dtype, SEED_BASE + 1, "cpu", w.d_skip, w.gate)
+    return {k: (oracle.f64(v) if v is not None else None) for k, v in inp.items()}
+
+
+def time_oracle_scan(w, target_s=12.0):
+    """Time the fp64 oracle on a bounded sample of workload w (all L steps of some batch rows
+    and channels, about target_s seconds). Returns (GB/s, seconds, sample, threads)."""
+    import oracle
+
+    rows, d, threads = _oracle_sample(w, target_s)
+    conv = _oracle_inputs(w, rows, d)
+    t0 = time.perf_counter()
+    oracle.ssm_scan_ref(**conv, nthreads=threads)
+    dt = time.perf_counter() - t0
+    nbytes = scan_bytes(w, batch=rows, dim=d)
+    return nbytes / dt / 1e9, dt, f"{rows} of {w.batch} batch rows, {d} of {w.dim} channels, all {w.seqlen} steps", threads
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def _timed(fn, steps, warmup, stream, barrier=None):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return e0.elapsed_time(e1) / steps  # ms per step
+
+
+def _max_over_ranks(v, dev, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], device=dev, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from selective_state_space_127_b300 import binding, ssd_chunk_scan_fwd, ssm_scan_fwd, ssm_scan_fwd_host
+    from selective_state_space_127_b300.synth import (SCAN_WORKLOADS, SSD_WORKLOAD, scan_workload_inputs,
+                                                      ssd_workload_inputs)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    barrier = (lambda: dist.barrier(device_ids=[local])) if world > 1 else None
+    binding.load_library()
+    peaks, peak_src = load_peaks()
+
+    w = SCAN_WORKLOADS[args.workload]
+    inp = scan_workload_inputs(args.workload, device=dev, rank=rank)
+    y = torch.empty_like(inp["x"])
+    hl = torch.empty(w.batch, w.dim, w.dstate, device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ssm_scan_fwd(**inp, out=y, h_last=hl, chunk_len=w.chunk_len)
+
+    clk = ClockSampler(local)
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    n0 = binding.kernel_launch_count()
+    tw0 = time.time()
+    ms = _timed(step, args.steps, 0, stream, barrier)
+    clk.mark(tw0, time.time())
+    launches = binding.kernel_launch_count() - n0
+    time.sleep(0.15)
+    clk.stop()
+    ms = _max_over_ranks(ms, dev, world)
+    nbytes = scan_bytes(w)
+    gbs_rank = nbytes / (ms * 1e-3) / 1e9
+    value = gbs_rank * world
+    updates = w.units
+    clocks = clk.summary()
+    mhz_peak = peaks.get("sm_max_mhz", 2032.0)
+    alu_peak = UPDATES_PER_CLK_SM * SMS * mhz_peak * 1e6 / 1e9   # G updates / s
+    achieved_upd = updates / (ms * 1e-3) / 1e9
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded torch generator on the device)",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "dim": w.dim, "dstate": w.dstate,
+                   "io_dtype": w.dtype, "state_dtype": "f32", "d_skip": True, "gate": True, "h_last": True,
+                   "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB per step > 126 MB); no flush",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_frac": round(gbs_rank / peaks["hbm_gbs"], 4),
+        "hbm_peak_gbs": peaks["hbm_gbs"], "peak_source": peak_src,
+        "roofline": {"bound": "alu", "achieved": round(achieved_upd, 1), "peak": round(alu_peak, 1),
+                     "unit": "Gupdate/s", "frac": round(achieved_upd / alu_peak, 4), "traffic": None,
+                     "kernel": "selective scan", "algorithmic_bytes": nbytes, "updates": updates,
+                     "peak_basis": f"{UPDATES_PER_CLK_SM:.0f} updates/clk/SM x {SMS} SMs x {mhz_peak:.0f} MHz "
+                                   "(ex2 and FP32-lane limits, measured)"},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+
+    if not args.no_ssd:
+        sw = SSD_WORKLOAD
+        sinp = ssd_workload_inputs(device=dev, rank=rank)
+        sy = torch.empty_like(sinp["x"])
+        shl = torch.empty(sw.batch, sw.nheads, sw.dstate, sw.headdim, device=dev, dtype=torch.float32)
+
+        def sstep():
+            ssd_chunk_scan_fwd(**sinp, chunk_size=sw.chunk, out=sy, h_last=shl)
+
+        ssteps = max(3, min(args.steps, 50))
+        sms = _max_over_ranks(_timed(sstep, ssteps, max(3, min(args.warmup, 5)), stream, barrier), dev, world)
+        fl = ssd_flops(sw)
+        tf = fl / (sms * 1e-3) / 1e12
+        result["ssd"] = {"workload": sw.name, "ms_per_step": round(sms, 4), "steps": ssteps,
+                         "value": round(tf * world, 3), "unit": "TFLOP/s", "flops_per_step": fl,
+                         "gbs": round(ssd_bytes(sw) / (sms * 1e-3) / 1e9 * world, 1),
+                         "tensor_frac_of_bf16_burst": round(tf / peaks["bf16_tflops"], 4)}
+        del sinp, sy, shl
+
+    if args.extra_workloads:
+        extra = {}
+        for k in (2, 3):
+            if k == args.workload:
+                continue
+            wk = SCAN_WORKLOADS[k]
+            kin = scan_workload_inputs(k, device=dev, rank=rank)
+            ky = torch.empty_like(kin["x"])
+            khl = torch.empty(wk.batch, wk.dim, wk.dstate, device=dev, dtype=torch.float32)
+            kms = _timed(lambda: ssm_scan_fwd(**kin, out=ky, h_last=khl, chunk_len=wk.chunk_len),
+                         max(3, min(args.steps, 20)), 3, stream, barrier)
+            kms = _max_over_ranks(kms, dev, world)
+            extra[str(k)] = {"workload": wk.name, "ms_per_step": round(kms, 4),
+                             "gbs": round(scan_bytes(wk) / (kms * 1e-3) / 1e9, 1),
+                             "hbm_frac": round(scan_bytes(wk) / (kms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+            del kin, ky, khl
+        result["extra_workloads"] = extra
+
+    if not args.no_e2e:
+        host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in inp.items()}
+        bufs = {}
+        for _ in range(2):
+            ssm_scan_fwd_host(host, device=dev, dev_buffers=bufs, chunk_len=w.chunk_len)
+        e2e_steps = max(3, min(args.steps, 10))
+        torch.cuda.synchronize()
+        if barrier:
+            barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            ssm_scan_fwd_host(host, device=dev, dev_buffers=bufs, chunk_len=w.chunk_len)
+        e2e_s = _max_over_ranks((time.perf_counter() - t0) / e2e_steps, dev, world)
+        h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+        d2h = y.numel() * y.element_size() + hl.numel() * hl.element_size()
+        result["e2e"] = {"value": round(nbytes / e2e_s / 1e9 * world, 2), "unit": "GB/s",
+                         "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                         "ms_per_step": round(e2e_s * 1e3, 3), "steps": e2e_steps,
+                         "api": "ssm_scan_fwd_host (pinned host in, pinned host out)"}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, secs, sample, threads = time_oracle_scan(w)
+        result["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                  "sample": sample, "seconds": round(secs, 2)}
+
+    if world > 1:
+        dist.barrier(device_ids=[local])
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from selective_state_space_127_b300.synth import SCAN_WORKLOADS
+
+    w = SCAN_WORKLOADS[args.workload]
+    # size one step so that warmup + steps stay within about three minutes
+    budget = min(10.0, 180.0 / max(1, args.steps + args.warmup))
+    rows, d, threads = _oracle_sample(w, budget)
+    conv = _oracle_inputs(w, rows, d)
+    for _ in range(args.warmup):
+        oracle.ssm_scan_ref(**conv, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.ssm_scan_ref(**conv, nthreads=threads)
+    dt = (time.perf_counter() - t0) / args.steps
+    nbytes = scan_bytes(w, batch=rows, dim=d)
+    gbs = nbytes / dt / 1e9
+    sample = f"{rows} of {w.batch} batch rows, {d} of {w.dim} channels, all {w.seqlen} steps (fp64 oracle)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

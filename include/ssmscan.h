@@ -6,7 +6,7 @@
  *  - Pointers in the params structs are DEVICE pointers owned by the caller; the library
  *    never allocates, frees or keeps them after the call returns.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Work is
- *    enqueued on it and the call returns without synchronising (except ssm_workspace_status).
+ *    enqueued on it and the call returns without synchronising (except ssm_device_status).
  *  - Argument errors are detected on the host before anything is launched and return
  *    SSM_ERR_INVALID_ARG (shape, stride, pointer, dtype or alignment problem) or
  *    SSM_ERR_UNSUPPORTED (a valid request this build does not implement); a one-line
@@ -43,7 +43,7 @@ typedef enum {
     SSM_ERR_INVALID_ARG = 1,
     SSM_ERR_UNSUPPORTED = 2,
     SSM_ERR_CUDA = 3,
-    SSM_ERR_TIMEOUT = 4,   /* a bounded device-side wait gave up (see ssm_workspace_status) */
+    SSM_ERR_TIMEOUT = 4,   /* a bounded device-side wait gave up (see ssm_device_status) */
     SSM_ERR_WORKSPACE = 5  /* workspace missing, too small or misaligned */
 } ssm_status_t;
 
@@ -57,6 +57,13 @@ typedef enum { SSM_DTYPE_F32 = 0, SSM_DTYPE_BF16 = 1 } ssm_dtype_t;
  *   ("State Space Model / Mamba", "Zero-Order Hold" and `discretize_zoh`; "Mamba/SSM
  *   complete guide" section 2 ZOH formula), with the limit delta * B where a == 0. */
 typedef enum { SSM_DISC_DELTA_B = 0, SSM_DISC_ZOH = 1 } ssm_discretization_t;
+
+/* Test hooks (debug_flags). SSM_DEBUG_SKIP_FIRST_LOAD: the TMA path never issues the copy
+ * of its first tile, so its bounded wait runs out (about one second), the kernel latches
+ * SSM_ERR_TIMEOUT in the device status word and returns with nothing in flight. Accepted
+ * only when the whole sequence fits in that first tile (L <= 32) and the TMA path applies;
+ * otherwise the call returns SSM_ERR_INVALID_ARG. */
+#define SSM_DEBUG_SKIP_FIRST_LOAD 1
 
 /*
  * Mamba-1 selective scan, one independent recurrence per (batch, channel):
@@ -102,6 +109,8 @@ typedef struct ssm_scan_params {
     void* workspace;        /* device scratch of ssm_scan_workspace_size() bytes, 256-byte
                                aligned; may be NULL when that size is 0 */
     size_t workspace_bytes;
+    int32_t debug_flags;    /* 0 in normal use; SSM_DEBUG_* test hooks */
+    int32_t reserved;       /* must be 0 */
 } ssm_scan_params;
 
 /* Bytes of device workspace ssm_scan_fwd needs for these params (0 if none). Host only,
@@ -156,10 +165,12 @@ SSMSCAN_API size_t ssd_chunk_scan_workspace_size(const ssd_scan_params* p);
 /* Enqueue the SSD chunked scan on `stream`. Returns SSM_OK once launched. */
 SSMSCAN_API ssm_status_t ssd_chunk_scan_fwd(const ssd_scan_params* p, void* stream);
 
-/* Synchronise `stream`, then report the device-side status word a kernel latched in
- * `workspace` (SSM_OK, or SSM_ERR_TIMEOUT when a bounded wait gave up). `workspace` must be
- * the buffer passed to the last call on that stream. NULL workspace reports SSM_OK. */
-SSMSCAN_API ssm_status_t ssm_workspace_status(const void* workspace, void* stream);
+/* Synchronise `stream`, then return the library's device status word for the current
+ * device: SSM_OK, or SSM_ERR_TIMEOUT if a kernel's bounded wait on its own TMA copies gave up
+ * since the word was last cleared (that kernel's outputs are then incomplete). With
+ * `clear` != 0 the word is reset to SSM_OK afterwards. Returns SSM_ERR_CUDA if the stream
+ * reports an error. */
+SSMSCAN_API ssm_status_t ssm_device_status(void* stream, int clear);
 
 /* Static, human-readable name of a status code. */
 SSMSCAN_API const char* ssm_status_string(ssm_status_t s);
@@ -169,6 +180,11 @@ SSMSCAN_API const char* ssm_last_error(void);
 
 /* SSMSCAN_ABI_VERSION of the library that was loaded. */
 SSMSCAN_API int ssm_abi_version(void);
+
+/* Number of kernels this library has enqueued in this process so far (all devices,
+ * all threads; copies and memsets are not counted). For benchmarks that report how many
+ * of the library's kernels ran in a timed region. */
+SSMSCAN_API uint64_t ssm_kernel_launch_count(void);
 
 #ifdef __cplusplus
 }

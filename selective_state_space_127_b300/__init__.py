@@ -4,7 +4,7 @@ The compute lives in libssmscan.so (CUDA for sm_103a, C ABI in include/ssmscan.h
 package holds its build script, a ctypes binding and the seeded input generators.
 """
 from .binding import (SSMError, load_library, ssd_chunk_scan_fwd, ssm_scan_fwd, ssm_scan_fwd_host,
-                      workspace_status)
+                      device_status)
 
 __all__ = ["SSMError", "load_library", "ssm_scan_fwd", "ssd_chunk_scan_fwd", "ssm_scan_fwd_host",
-           "workspace_status"]
+           "device_status"]

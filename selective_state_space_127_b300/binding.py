@@ -24,7 +24,8 @@ ABI_VERSION = 1
 
 # Every function the header declares (checked by the CPU test suite).
 EXPORTS = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssd_chunk_scan_workspace_size", "ssd_chunk_scan_fwd",
-           "ssm_workspace_status", "ssm_status_string", "ssm_last_error", "ssm_abi_version")
+           "ssm_device_status", "ssm_status_string", "ssm_last_error", "ssm_abi_version",
+           "ssm_kernel_launch_count")
 
 _i64, _i32, _vp, _sz = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
 
@@ -36,7 +37,10 @@ class ScanParams(ctypes.Structure):
                 ("A", _vp), ("D", _vp), ("delta_bias", _vp), ("h0", _vp), ("y", _vp), ("h_last", _vp),
                 ("x_stride", _i64 * 3), ("delta_stride", _i64 * 3), ("z_stride", _i64 * 3),
                 ("y_stride", _i64 * 3), ("B_stride", _i64 * 3), ("C_stride", _i64 * 3),
-                ("chunk_len", _i64), ("workspace", _vp), ("workspace_bytes", _sz)]
+                ("chunk_len", _i64), ("workspace", _vp), ("workspace_bytes", _sz),
+                ("debug_flags", _i32), ("reserved", _i32)]
+
+SSM_DEBUG_SKIP_FIRST_LOAD = 1
 
 
 class SSDParams(ctypes.Structure):
@@ -74,14 +78,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.ssd_chunk_scan_workspace_size.restype = _sz
             lib.ssd_chunk_scan_fwd.argtypes = [ctypes.POINTER(SSDParams), _vp]
             lib.ssd_chunk_scan_fwd.restype = ctypes.c_int
-            lib.ssm_workspace_status.argtypes = [_vp, _vp]
-            lib.ssm_workspace_status.restype = ctypes.c_int
+            lib.ssm_device_status.argtypes = [_vp, ctypes.c_int]
+            lib.ssm_device_status.restype = ctypes.c_int
             lib.ssm_status_string.argtypes = [ctypes.c_int]
             lib.ssm_status_string.restype = ctypes.c_char_p
             lib.ssm_last_error.argtypes = []
             lib.ssm_last_error.restype = ctypes.c_char_p
             lib.ssm_abi_version.argtypes = []
             lib.ssm_abi_version.restype = ctypes.c_int
+            lib.ssm_kernel_launch_count.argtypes = []
+            lib.ssm_kernel_launch_count.restype = ctypes.c_uint64
             if lib.ssm_abi_version() != ABI_VERSION:
                 raise RuntimeError(f"{path}: ABI version {lib.ssm_abi_version()} != {ABI_VERSION}")
             _lib = lib
@@ -133,7 +139,7 @@ def _stream_handle(stream) -> int:
 
 def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_softplus=True, h0=None,
                  reverse=False, zoh=False, chunk_len=0, out=None, return_last_state=True, h_last=None,
-                 stream=None):
+                 stream=None, debug_flags=0):
     """Selective scan on the GPU. x, delta, z: (b, L, D); B, C: (b, L, N); A: (D, N) fp32;
     D, delta_bias: (D) fp32; h0: (b, D, N) fp32. I/O tensors are fp32 or bf16 (all alike) and
     may be strided (delta's channel stride may be 0). Returns (y, h_last or None)."""
@@ -176,6 +182,7 @@ def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_so
     p.B_stride[:] = _strides3(B)
     p.C_stride[:] = _strides3(C)
     p.chunk_len = int(chunk_len)
+    p.debug_flags = int(debug_flags)
     ws_bytes = lib.ssm_scan_workspace_size(ctypes.byref(p))
     if ws_bytes == ctypes.c_size_t(-1).value:
         _check(lib, lib.ssm_scan_fwd(ctypes.byref(p), None))  # raises with the reason
@@ -264,7 +271,13 @@ def ssm_scan_fwd_host(inputs: dict, device="cuda", stream=None, dev_buffers: dic
     return y_host, hl_host
 
 
-def workspace_status(workspace: torch.Tensor | None, stream=None) -> int:
-    """Synchronise the stream and return the device-side status the last call latched."""
+def kernel_launch_count() -> int:
+    """Kernels the library has enqueued in this process so far."""
+    return int(load_library().ssm_kernel_launch_count())
+
+
+def device_status(clear: bool = True, stream=None) -> int:
+    """Synchronise the stream and return the library's device status word (SSM_OK or
+    SSM_ERR_TIMEOUT), clearing it by default."""
     lib = load_library()
-    return lib.ssm_workspace_status(_ptr(workspace), _stream_handle(stream))
+    return lib.ssm_device_status(_stream_handle(stream), int(bool(clear)))

@@ -3,12 +3,18 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 
 #include "internal.h"
 #include "ssmscan.h"
+
+namespace ssm {
+static std::atomic<uint64_t> g_launches{0};
+void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+}  // namespace ssm
 
 namespace {
 
@@ -78,6 +84,8 @@ ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
     if ((p->delta_softplus != 0 && p->delta_softplus != 1) || (p->reverse != 0 && p->reverse != 1))
         return fail(SSM_ERR_INVALID_ARG, "delta_softplus and reverse must be 0 or 1");
     if (p->chunk_len < 0) return fail(SSM_ERR_INVALID_ARG, "chunk_len must be >= 0");
+    if (p->reserved != 0 || (p->debug_flags & ~SSM_DEBUG_SKIP_FIRST_LOAD) != 0)
+        return fail(SSM_ERR_INVALID_ARG, "unknown debug_flags or nonzero reserved field");
     if (!p->A) return fail(SSM_ERR_INVALID_ARG, "A is NULL");
     if (p->seqlen > 0 && (!p->x || !p->delta || !p->B || !p->C || !p->y))
         return fail(SSM_ERR_INVALID_ARG, "x, delta, B, C and y are required");
@@ -131,6 +139,7 @@ ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
     a.chunk_len = p->chunk_len;
     a.workspace = p->workspace;
     a.workspace_bytes = p->workspace_bytes;
+    a.debug_flags = p->debug_flags;
     return SSM_OK;
 }
 
@@ -211,6 +220,8 @@ ssm_status_t ssm_scan_fwd(const ssm_scan_params* p, void* stream) {
         return fail(SSM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
+    if ((a.debug_flags & SSM_DEBUG_SKIP_FIRST_LOAD) && (a.seqlen < 1 || a.seqlen > 32 || !ssm::scan_fast_supported(a)))
+        return fail(SSM_ERR_INVALID_ARG, "SSM_DEBUG_SKIP_FIRST_LOAD needs 1 <= seqlen <= 32 and the TMA path");
     if (a.seqlen == 0) {
         if (a.h_last) {
             const size_t bytes = (size_t)(a.batch * a.dim * a.dstate) * sizeof(float);
@@ -218,6 +229,8 @@ ssm_status_t ssm_scan_fwd(const ssm_scan_params* p, void* stream) {
                                          : cudaMemcpyAsync(a.h_last, a.h0, bytes, cudaMemcpyDeviceToDevice, st))
                      : cudaMemsetAsync(a.h_last, 0, bytes, st);
         }
+    } else if (ssm::scan_fast_supported(a)) {
+        e = ssm::launch_scan_fast(a, st);
     } else {
         e = ssm::launch_scan_generic(a, st);
     }
@@ -241,15 +254,11 @@ ssm_status_t ssd_chunk_scan_fwd(const ssd_scan_params* p, void* stream) {
     return ok();
 }
 
-ssm_status_t ssm_workspace_status(const void* workspace, void* stream) {
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaStreamSynchronize(st);
+ssm_status_t ssm_device_status(void* stream, int clear) {
+    unsigned word = 0;
+    cudaError_t e = ssm::read_device_status(&word, clear != 0, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
-    if (!workspace) return ok();
-    uint32_t word = 0;
-    e = cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (word != 0) return fail(SSM_ERR_TIMEOUT, "device status word %u", word);
+    if (word != 0) return fail(static_cast<ssm_status_t>(word), "a kernel latched device status %u", word);
     return ok();
 }
 
@@ -268,5 +277,7 @@ const char* ssm_status_string(ssm_status_t s) {
 const char* ssm_last_error(void) { return g_last_error; }
 
 int ssm_abi_version(void) { return SSMSCAN_ABI_VERSION; }
+
+uint64_t ssm_kernel_launch_count(void) { return ssm::g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

@@ -29,6 +29,7 @@ struct ScanArgs {
     int64_t chunk_len;
     void* workspace;
     size_t workspace_bytes;
+    int debug_flags;
 };
 
 struct SSDArgs {
@@ -53,8 +54,18 @@ struct SSDArgs {
 // Which selective-scan kernel a call takes.
 enum class ScanPath { Generic = 0, Fast = 1, ChunkCarry = 2 };
 
+// Count of kernels enqueued by this library (reported through ssm_kernel_launch_count).
+void note_launches(int n);
+
+// Device address of the library's status word on the current device (nullptr on error).
+// Kernels latch SSM_ERR_TIMEOUT there when a bounded wait gives up.
+unsigned* device_status_ptr();
+cudaError_t read_device_status(unsigned* out, bool clear, cudaStream_t st);
+
 // Kernel launchers: return cudaSuccess or the launch error. They assume valid args.
 cudaError_t launch_scan_generic(const ScanArgs& a, cudaStream_t s);
+bool scan_fast_supported(const ScanArgs& a);
+cudaError_t launch_scan_fast(const ScanArgs& a, cudaStream_t s);
 cudaError_t launch_ssd_reference(const SSDArgs& a, cudaStream_t s);
 
 }  // namespace ssm

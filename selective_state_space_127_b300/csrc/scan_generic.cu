@@ -93,6 +93,7 @@ cudaError_t launch(const ScanArgs& a, cudaStream_t st) {
     const int64_t per_block = kGenericThreads / G;
     const int64_t grid = (nchan + per_block - 1) / per_block;
     scan_generic_kernel<S, G><<<(unsigned)grid, kGenericThreads, 0, st>>>(a);
+    note_launches(1);
     return cudaGetLastError();
 }
 

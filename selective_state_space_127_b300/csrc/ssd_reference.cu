@@ -94,6 +94,7 @@ cudaError_t launch_ssd_reference(const SSDArgs& a, cudaStream_t st) {
     const int J = kRefThreads / P;
     const size_t smem = (size_t)(2 * N + J * P) * sizeof(float);
     ssd_reference_kernel<<<(unsigned)(a.batch * a.nheads), kRefThreads, smem, st>>>(a);
+    note_launches(1);
     return cudaGetLastError();
 }
 

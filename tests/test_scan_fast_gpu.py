@@ -1,0 +1,95 @@
+"""GPU tests of the TMA selective-scan path: parity with the oracle on layouts it takes,
+agreement with the generic path, and the bounded-wait timeout (host-injected, no fault)."""
+import pytest
+import torch
+
+import oracle
+from selective_state_space_127_b300 import binding, device_status, ssm_scan_fwd
+from selective_state_space_127_b300.synth import make_scan_inputs
+from conftest import rel_l2
+
+pytestmark = pytest.mark.gpu
+
+TOL_Y = {"f32": 1e-5, "bf16": 2e-2}
+TOL_H = {"f32": 1e-5, "bf16": 1e-4}
+
+
+def _to(dev, inp):
+    return {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+
+
+def _misaligned_copy(t):
+    """Same values in a view whose base is off the 16-byte grid (the TMA path refuses it)."""
+    big = torch.empty(t.shape[:-1] + (t.shape[-1] + 1,), dtype=t.dtype, device=t.device)
+    v = big[..., 1:]
+    v.copy_(t)
+    return v
+
+
+FAST_CASES = [
+    # b, L, D, N, dtype, gate, dskip, softplus
+    (1, 1, 16, 16, "bf16", True, True, True),
+    (2, 77, 40, 16, "bf16", True, True, True),
+    (3, 300, 48, 64, "f32", True, False, True),
+    (1, 70, 32, 64, "bf16", True, True, True),
+    (1, 129, 24, 32, "bf16", False, True, True),
+    (2, 64, 64, 16, "f32", False, False, True),
+    (1, 1000, 16, 16, "bf16", True, True, True),
+    (2, 45, 32, 32, "f32", True, True, False),
+]
+
+
+@pytest.mark.parametrize("b,L,D,N,dt,gate,dskip,sp", FAST_CASES)
+def test_tma_path_matches_oracle_and_generic_path(cuda_dev, b, L, D, N, dt, gate, dskip, sp):
+    inp = make_scan_inputs(b, L, D, N, dt, seed=3000 + L + D + N, d_skip="normal" if dskip else "none", gate=gate)
+    if not sp:
+        inp["delta"] = (inp["delta"].float().abs() * 0.05).to(inp["delta"].dtype)
+        inp["delta_bias"] = torch.full_like(inp["delta_bias"], 1e-3)
+    g = _to(cuda_dev, inp)
+    y_fast, h_fast = ssm_scan_fwd(**g, delta_softplus=sp)
+    slow = dict(g, x=_misaligned_copy(g["x"]))
+    y_gen, h_gen = ssm_scan_fwd(**slow, delta_softplus=sp)
+    torch.cuda.synchronize()
+    y_ref, h_ref = oracle.ssm_scan_ref(**inp, delta_softplus=sp)
+    yf, yg = y_fast.float().cpu().numpy(), y_gen.float().cpu().numpy()
+    assert rel_l2(yf, y_ref) <= TOL_Y[dt]
+    assert rel_l2(h_fast.cpu().numpy(), h_ref) <= TOL_H[dt]
+    assert rel_l2(yg, y_ref) <= TOL_Y[dt]
+    # same fp32 recurrence, different softplus evaluation and summation order
+    assert rel_l2(h_fast.cpu().numpy(), h_gen.cpu().numpy()) <= 2e-6
+    assert device_status() == binding.SSM_OK
+
+
+def test_bf16_outputs_are_the_rounded_oracle(cuda_dev):
+    """With fp32 state the only visible error on bf16 y should be the final rounding: nearly
+    every element equals the oracle's value rounded to bf16, and the rest differ by one bf16
+    step (or by fp32-level noise where y is near zero)."""
+    inp = make_scan_inputs(4, 512, 256, 16, "bf16", seed=99)
+    y, _ = ssm_scan_fwd(**_to(cuda_dev, inp))
+    y_ref, _ = oracle.ssm_scan_ref(**inp)
+    y_ref_b = torch.from_numpy(y_ref).to(torch.bfloat16)
+    same = (y.cpu() == y_ref_b).float().mean().item()
+    scale = float(torch.from_numpy(y_ref).pow(2).mean().sqrt())
+    near = (y.cpu().float() - y_ref_b.float()).abs() <= y_ref_b.float().abs() * 2 ** -7 + 1e-5 * scale
+    assert same >= 0.97, same
+    assert near.all()
+
+
+def test_injected_missing_copy_times_out_and_context_survives(cuda_dev):
+    """The test hook withholds the first TMA copy: the bounded wait gives up after about a
+    second, the status word reads SSM_ERR_TIMEOUT, and the next call works normally."""
+    inp = _to(cuda_dev, make_scan_inputs(1, 20, 32, 16, "bf16", seed=5))
+    assert device_status() == binding.SSM_OK
+    ssm_scan_fwd(**inp, debug_flags=binding.SSM_DEBUG_SKIP_FIRST_LOAD)
+    assert device_status(clear=True) == binding.SSM_ERR_TIMEOUT
+    assert device_status() == binding.SSM_OK
+    y, h = ssm_scan_fwd(**inp)
+    y_ref, h_ref = oracle.ssm_scan_ref(**{k: (v.cpu() if v is not None else None) for k, v in inp.items()})
+    assert rel_l2(y.float().cpu().numpy(), y_ref) <= TOL_Y["bf16"]
+
+
+def test_debug_hook_is_refused_where_it_could_leave_copies_in_flight(cuda_dev):
+    inp = _to(cuda_dev, make_scan_inputs(1, 100, 32, 16, "bf16", seed=6))
+    with pytest.raises(binding.SSMError) as e:
+        ssm_scan_fwd(**inp, debug_flags=binding.SSM_DEBUG_SKIP_FIRST_LOAD)
+    assert e.value.status == binding.SSM_ERR_INVALID_ARG
