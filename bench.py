@@ -260,8 +260,11 @@ def run_ours(args):
     hl = torch.empty(w.batch, w.dim, w.dstate, device=dev, dtype=torch.float32)
     stream = torch.cuda.current_stream()
 
+    ws = torch.empty(max(1, binding.scan_workspace_size(**inp, chunk_len=w.chunk_len)), device=dev,
+                     dtype=torch.uint8)
+
     def step():
-        ssm_scan_fwd(**inp, out=y, h_last=hl, chunk_len=w.chunk_len)
+        ssm_scan_fwd(**inp, out=y, h_last=hl, chunk_len=w.chunk_len, workspace=ws)
 
     clk = ClockSampler(local)
     time.sleep(0.3)
@@ -331,7 +334,9 @@ def run_ours(args):
             kin = scan_workload_inputs(k, device=dev, rank=rank)
             ky = torch.empty_like(kin["x"])
             khl = torch.empty(wk.batch, wk.dim, wk.dstate, device=dev, dtype=torch.float32)
-            kms = _timed(lambda: ssm_scan_fwd(**kin, out=ky, h_last=khl, chunk_len=wk.chunk_len),
+            kws = torch.empty(max(1, binding.scan_workspace_size(**kin, chunk_len=wk.chunk_len)), device=dev,
+                              dtype=torch.uint8)
+            kms = _timed(lambda: ssm_scan_fwd(**kin, out=ky, h_last=khl, chunk_len=wk.chunk_len, workspace=kws),
                          max(3, min(args.steps, 20)), 3, stream, barrier)
             kms = _max_over_ranks(kms, dev, world)
             extra[str(k)] = {"workload": wk.name, "ms_per_step": round(kms, 4),

@@ -61,7 +61,7 @@ typedef enum { SSM_DISC_DELTA_B = 0, SSM_DISC_ZOH = 1 } ssm_discretization_t;
 /* Test hooks (debug_flags). SSM_DEBUG_SKIP_FIRST_LOAD: the TMA path never issues the copy
  * of its first tile, so its bounded wait runs out (about one second), the kernel latches
  * SSM_ERR_TIMEOUT in the device status word and returns with nothing in flight. Accepted
- * only when the whole sequence fits in that first tile (L <= 32) and the TMA path applies;
+ * only when the whole sequence fits in that first tile (L <= 16) and the TMA path applies;
  * otherwise the call returns SSM_ERR_INVALID_ARG. */
 #define SSM_DEBUG_SKIP_FIRST_LOAD 1
 
@@ -105,7 +105,11 @@ typedef struct ssm_scan_params {
     int64_t y_stride[3];    /* y must not broadcast: all strides > 0 unless the size is 1 */
     int64_t B_stride[3];    /* (b, t, n) */
     int64_t C_stride[3];
-    int64_t chunk_len;      /* time-chunk length for the chunk-carry path; 0 = choose */
+    int64_t chunk_len;      /* steps per chunk when the sequence is split across CTAs (the TMA
+                               path rounds it up to a multiple of 16; >= L or a path that does
+                               not split: one chunk); 0 = let the library choose. The result does
+                               not depend on it beyond fp32 rounding. With more than one chunk the
+                               call needs (nchunks - 1) * b * D * (N + 1) * 4 bytes of workspace. */
     void* workspace;        /* device scratch of ssm_scan_workspace_size() bytes, 256-byte
                                aligned; may be NULL when that size is 0 */
     size_t workspace_bytes;

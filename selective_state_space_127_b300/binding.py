@@ -137,13 +137,10 @@ def _stream_handle(stream) -> int:
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_softplus=True, h0=None,
+def _scan_params(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_softplus=True, h0=None,
                  reverse=False, zoh=False, chunk_len=0, out=None, return_last_state=True, h_last=None,
-                 stream=None, debug_flags=0):
-    """Selective scan on the GPU. x, delta, z: (b, L, D); B, C: (b, L, N); A: (D, N) fp32;
-    D, delta_bias: (D) fp32; h0: (b, D, N) fp32. I/O tensors are fp32 or bf16 (all alike) and
-    may be strided (delta's channel stride may be 0). Returns (y, h_last or None)."""
-    lib = load_library()
+                 debug_flags=0):
+    """Check the tensors and fill a ScanParams; returns (params, y, h_last)."""
     if not x.is_cuda:
         raise ValueError("x must be a CUDA tensor (use ssm_scan_fwd_host for host buffers)")
     dev = x.device
@@ -183,14 +180,41 @@ def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_so
     p.C_stride[:] = _strides3(C)
     p.chunk_len = int(chunk_len)
     p.debug_flags = int(debug_flags)
+    return p, y, hl
+
+
+def scan_workspace_size(x, delta, A, B, C, D=None, z=None, delta_bias=None, **kw) -> int:
+    """Bytes of device workspace ssm_scan_fwd needs for these arguments (0 if none)."""
+    lib = load_library()
+    kw = {k: v for k, v in kw.items() if k not in ("stream", "workspace")}
+    p, _, _ = _scan_params(x, delta, A, B, C, D, z, delta_bias, **kw)
+    n = lib.ssm_scan_workspace_size(ctypes.byref(p))
+    if n == ctypes.c_size_t(-1).value:
+        _check(lib, lib.ssm_scan_fwd(ctypes.byref(p), None))  # raises with the reason
+    return int(n)
+
+
+def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_softplus=True, h0=None,
+                 reverse=False, zoh=False, chunk_len=0, out=None, return_last_state=True, h_last=None,
+                 stream=None, workspace=None, debug_flags=0):
+    """Selective scan on the GPU. x, delta, z: (b, L, D); B, C: (b, L, N); A: (D, N) fp32;
+    D, delta_bias: (D) fp32; h0: (b, D, N) fp32. I/O tensors are fp32 or bf16 (all alike) and
+    may be strided (delta's channel stride may be 0). ``workspace`` (a uint8 CUDA tensor of at
+    least scan_workspace_size() bytes, 256-byte aligned) is allocated when not given.
+    Returns (y, h_last or None)."""
+    lib = load_library()
+    p, y, hl = _scan_params(x, delta, A, B, C, D, z, delta_bias, delta_softplus=delta_softplus, h0=h0,
+                            reverse=reverse, zoh=zoh, chunk_len=chunk_len, out=out,
+                            return_last_state=return_last_state, h_last=h_last, debug_flags=debug_flags)
     ws_bytes = lib.ssm_scan_workspace_size(ctypes.byref(p))
     if ws_bytes == ctypes.c_size_t(-1).value:
         _check(lib, lib.ssm_scan_fwd(ctypes.byref(p), None))  # raises with the reason
-    ws = None
     if ws_bytes > 0:
-        ws = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
-        p.workspace, p.workspace_bytes = _ptr(ws), ws_bytes
-    with torch.cuda.device(dev):
+        ws = workspace
+        if ws is None or ws.numel() < ws_bytes:
+            ws = torch.empty(ws_bytes, device=x.device, dtype=torch.uint8)
+        p.workspace, p.workspace_bytes = _ptr(ws), ws.numel()
+    with torch.cuda.device(x.device):
         _check(lib, lib.ssm_scan_fwd(ctypes.byref(p), _stream_handle(stream)))
     return y, hl
 

@@ -143,7 +143,9 @@ ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
     return SSM_OK;
 }
 
-size_t scan_workspace_bytes(const ssm::ScanArgs&) { return 0; }
+size_t scan_workspace_bytes(const ssm::ScanArgs& a) {
+    return ssm::scan_fast_supported(a) ? ssm::scan_fast_workspace_bytes(a) : 0;
+}
 
 ssm_status_t cuda_fail(cudaError_t e) {
     return fail(SSM_ERR_CUDA, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
@@ -220,8 +222,8 @@ ssm_status_t ssm_scan_fwd(const ssm_scan_params* p, void* stream) {
         return fail(SSM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
-    if ((a.debug_flags & SSM_DEBUG_SKIP_FIRST_LOAD) && (a.seqlen < 1 || a.seqlen > 32 || !ssm::scan_fast_supported(a)))
-        return fail(SSM_ERR_INVALID_ARG, "SSM_DEBUG_SKIP_FIRST_LOAD needs 1 <= seqlen <= 32 and the TMA path");
+    if ((a.debug_flags & SSM_DEBUG_SKIP_FIRST_LOAD) && (a.seqlen < 1 || a.seqlen > 16 || !ssm::scan_fast_supported(a)))
+        return fail(SSM_ERR_INVALID_ARG, "SSM_DEBUG_SKIP_FIRST_LOAD needs 1 <= seqlen <= 16 and the TMA path");
     if (a.seqlen == 0) {
         if (a.h_last) {
             const size_t bytes = (size_t)(a.batch * a.dim * a.dstate) * sizeof(float);
@@ -249,7 +251,19 @@ ssm_status_t ssd_chunk_scan_fwd(const ssd_scan_params* p, void* stream) {
     ssm_status_t s = validate_ssd(p, &a);
     if (s != SSM_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = ssm::launch_ssd_reference(a, st);
+    cudaError_t e = cudaSuccess;
+    if (a.seqlen == 0) {
+        if (a.h_last) {
+            const size_t bytes = (size_t)(a.batch * a.nheads * a.dstate * a.headdim) * sizeof(float);
+            e = a.h0 ? (a.h0 == a.h_last ? cudaSuccess
+                                         : cudaMemcpyAsync(a.h_last, a.h0, bytes, cudaMemcpyDeviceToDevice, st))
+                     : cudaMemsetAsync(a.h_last, 0, bytes, st);
+        }
+    } else if (ssm::ssd_tc_supported(a)) {
+        e = ssm::launch_ssd_tc(a, st);
+    } else {
+        e = ssm::launch_ssd_reference(a, st);
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     return ok();
 }

@@ -65,7 +65,14 @@ cudaError_t read_device_status(unsigned* out, bool clear, cudaStream_t st);
 // Kernel launchers: return cudaSuccess or the launch error. They assume valid args.
 cudaError_t launch_scan_generic(const ScanArgs& a, cudaStream_t s);
 bool scan_fast_supported(const ScanArgs& a);
+// Steps per chunk the fast path uses (a multiple of its tile; >= seqlen when not split) and
+// the workspace it needs for the chunk carries (0 when the sequence is not split).
+int64_t scan_fast_chunk(const ScanArgs& a);
+size_t scan_fast_workspace_bytes(const ScanArgs& a);
 cudaError_t launch_scan_fast(const ScanArgs& a, cudaStream_t s);
 cudaError_t launch_ssd_reference(const SSDArgs& a, cudaStream_t s);
+// Tensor-core SSD path: bf16 I/O, P = 64, N = 128, chunk a multiple of 128, TMA-aligned.
+bool ssd_tc_supported(const SSDArgs& a);
+cudaError_t launch_ssd_tc(const SSDArgs& a, cudaStream_t s);
 
 }  // namespace ssm

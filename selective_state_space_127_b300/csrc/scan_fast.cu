@@ -1,32 +1,44 @@
-// Fast selective-scan kernel for dense channel-contiguous layouts (the Mamba block's
+// Fast selective-scan kernels for dense channel-contiguous layouts (the Mamba block's
 // (b, L, D) activations and (b, L, N) B, C), N in {16, 32, 64}, forward direction,
-// delta*B discretisation.
+// delta*B discretisation; with an optional split of the sequence into chunks.
 //
-// Work split. A CTA is two warps and owns 16 consecutive channels of one batch row for the
-// whole sequence; four lanes 4c..4c+3 share channel c, each holding N/4 fp32 states in
-// registers (config b8 D1536 N16: 1536 warps, ~10 per SM, 4 states per lane).
+// Work split. A CTA owns kCh = 16 consecutive channels of one batch row and walks one
+// chunk of the sequence (the whole sequence when it is not split). LPC lanes share a
+// channel, each keeping N / LPC fp32 states in registers.
 //
-// Data movement. TMA (3-D tensor maps over (D or N, L, b)) streams 32-step tiles of x,
-// delta, z, B and C into a 3-deep shared-memory ring guarded by mbarriers; y tiles leave
-// through TMA stores from a double buffer. B and C tiles are widened to fp32 once per stage
-// by the CTA, so every lane then reads its N/4 values with 16-byte loads.
+// Per tile of kT = 16 steps:
+//  1. TMA (3-D maps over (D or N, L, b)) has brought x, delta, z, B and C into a kStages
+//     ring guarded by mbarriers.
+//  2. Producer phase, all threads: for each (step, channel) the scalars that do not depend
+//     on the state, dt = softplus(delta + bias), u = dt x, silu(z) and D x, computed once
+//     (two channels per thread) and written to shared memory as (dt, dt, u, u) and
+//     (D x, silu z); B and C are widened to fp32. The ring slot is then refilled.
+//  3. Update phase: lane g of channel c, per step, reads (dt, dt, u, u) and its B, C
+//     slices with 16-byte loads and runs, on packed fp32 pairs (f32x2),
+//        A_bar = 2^(dt * A log2 e)            SFU ex2, one per state
+//        h     = A_bar h + u B                fma.rn.f32x2 / mul.rn.f32x2
+//        y    += C h
+//     then the LPC lanes' partial sums of LPC consecutive steps are reduce-scattered with
+//     shuffles so lane g finishes step g as (y + D x) silu(z); y leaves by TMA store.
 //
-// Steps go in groups of four. Lane g of a channel computes the per-(t, channel) scalars of
-// step g of the group (softplus(delta + bias), dt x, silu(z)) one group ahead, so that
-// chain overlaps the state updates of the current group; the four (dt, dt x) pairs are then
-// broadcast inside the channel's lanes. Per step and state:
-//   A_bar[n] = 2^(dt * A[n] * log2 e)           SFU ex2
-//   h[n] = A_bar[n] h[n] + (dt x) B[n]          packed fp32 pairs (fma.rn.f32x2)
-//   y += C[n] h[n]                               packed pairs
-// and the four lanes' partial sums of the four steps are reduce-scattered (two shuffle
-// rounds), leaving lane g with step g's y, which it finishes as (y + D x) silu(z).
+// Chunked sequence (long sequences with few channels, where one CTA per channel tile
+// would leave most SMs idle):
+//  * pass 1 (kPass1): every chunk but the last runs from a zero state without the readout
+//    and writes its local end state and the sum of its dt (per channel) to the workspace;
+//  * carry kernel: per (b, d, n), H_0 = h0, H_{c+1} = exp(A sum_dt_c) H_c + local_c, in
+//    chunk order, written back in place as the initial state of chunk c + 1;
+//  * pass 2 (kFull): every chunk runs from its initial state and writes y; the last chunk
+//    also writes h_last.
+// The split uses the associativity of the recurrence h -> A_bar h + b: a chunk's map is
+// h -> (prod A_bar) h + (its zero-start end state), and prod A_bar = exp(A sum dt).
 //
 // Recurrence: "Mamba/SSM complete guide" section 5 `selective_scan` and MambaBlock.forward;
 // "論文解説: Mamba" "選択機構" (softplus) and "Hardware-Aware Parallel Scan" (state kept
-// on chip, only the outputs written back).
+// on chip, only the outputs written back; the parallel scan over (A_bar, B_bar x) pairs).
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -37,21 +49,25 @@ namespace ssm {
 namespace {
 
 constexpr int kCh = 16;        // channels per CTA
-constexpr int kG = 4;          // lanes per channel
-constexpr int kThreads = kCh * kG;
-constexpr int kT = 32;         // steps per stage
-constexpr int kStages = 3;     // TMA ring depth
+constexpr int kT = 16;         // steps per tile
+constexpr int kStages = 4;     // TMA ring depth
+
+enum Mode { kFull = 0, kPass1 = 1 };
 
 struct FastParams {
     int64_t seqlen;
+    int64_t chunk;         // steps per chunk (multiple of kT); >= seqlen when not split
     int dim;
+    int nchunks;
     const float* A;
     const float* D;
     const float* bias;
     const float* h0;
     float* h_last;
+    float* carry;          // (nchunks - 1, b, D, N): local end states, then initial states
+    float* sumdt;          // (nchunks - 1, b, D)
     unsigned* status;
-    int skip_first_load;   // test hook: never issue stage 0 (only used when the sequence is one stage)
+    int skip_first_load;   // test hook: never issue tile 0 (only used when the sequence is one tile)
 };
 
 template <int N, bool BF16>
@@ -63,15 +79,26 @@ struct Layout {
     static constexpr int kStageStride = (kStageBytes + 127) / 128 * 128;
     static constexpr int kBars = 0;                                   // kStages mbarriers
     static constexpr int kRing = 128;
-    static constexpr int kBCf = kRing + kStages * kStageStride;       // fp32 B, C (bf16 I/O)
-    static constexpr int kBCfBytes = BF16 ? 2 * kT * N * 4 : 0;
-    static constexpr int kY = kBCf + (kBCfBytes + 127) / 128 * 128;   // 2 y tiles
+    static constexpr int kSc = kRing + kStages * kStageStride;        // float4 (dt, dt, u, u) [kT][kCh]
+    static constexpr int kEg = kSc + kT * kCh * 16;                   // float2 (D x, silu z) [kT][kCh]
+    static constexpr int kBCf = kEg + kT * kCh * 8;                   // fp32 B then C [kT][N]
+    static constexpr int kY = kBCf + 2 * kT * N * 4;                  // 2 y tiles
     static constexpr int kYStride = (kTileX + 127) / 128 * 128;
     static constexpr int kTotal = kY + 2 * kYStride;
 };
 
-__device__ __forceinline__ float ld_io(const void* base, int i, bool bf16) {
-    return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]) : static_cast<const float*>(base)[i];
+// Two consecutive I/O elements (bf16 or fp32) of a shared-memory tile as floats.
+template <bool BF16>
+__device__ __forceinline__ void ld_pair(const unsigned char* tile, int idx, float& a, float& b) {
+    if constexpr (BF16) {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(tile + idx * 2);
+        a = __uint_as_float(v << 16);
+        b = __uint_as_float(v & 0xffff0000u);
+    } else {
+        const float2 v = *reinterpret_cast<const float2*>(tile + idx * 4);
+        a = v.x;
+        b = v.y;
+    }
 }
 
 // Sixteen bytes of shared memory as two packed fp32 pairs.
@@ -81,46 +108,47 @@ __device__ __forceinline__ void lds_2xf2(const float* p, f2& lo, f2& hi) {
     hi = v.y;
 }
 
-// Per-(step, channel) scalars one lane computes for its step of a group.
-struct Scal {
-    float dt, u, xr, gate;
-};
-
-template <bool BF16, bool GATE, bool SOFTPLUS>
-__device__ __forceinline__ Scal scalars(const void* xs, const void* ds, const void* zs, int jj, int c, float bias,
-                                        bool tv) {
-    Scal r;
-    r.xr = ld_io(xs, jj * kCh + c, BF16);
-    float dt = ld_io(ds, jj * kCh + c, BF16) + bias;
-    if constexpr (SOFTPLUS) dt = softplus_fast(dt);
-    r.dt = tv ? dt : 0.f;
-    r.u = r.dt * r.xr;
-    r.gate = GATE ? silu_fast(ld_io(zs, jj * kCh + c, BF16)) : 1.f;
-    return r;
-}
-
-template <int N, bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS>
-__global__ void __launch_bounds__(kThreads)
+template <int N, bool BF16, int LPC, bool GATE, bool DSKIP, bool SOFTPLUS, int MODE>
+__global__ void __launch_bounds__(kCh * LPC)
 scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap md,
                  const __grid_constant__ CUtensorMap mz, const __grid_constant__ CUtensorMap mB,
                  const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap my,
                  const FastParams p) {
     using Lay = Layout<N, BF16>;
-    constexpr int S = N / kG;          // states per lane
+    constexpr int kThreads = kCh * LPC;
+    constexpr int S = N / LPC;         // states per lane
     constexpr int P = S / 2;           // packed pairs per lane
+    constexpr bool kReadout = MODE == kFull;
+    constexpr bool kGate = GATE && kReadout;
     static_assert(S % 4 == 0, "states per lane must be a multiple of 4");
+    static_assert(LPC == 2 || LPC == 4, "2 or 4 lanes per channel");
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBars);
+    float4* sc = reinterpret_cast<float4*>(smem + Lay::kSc);
+    float2* eg = reinterpret_cast<float2*>(smem + Lay::kEg);
+    float* bcf = reinterpret_cast<float*>(smem + Lay::kBCf);
 
     const int tid = threadIdx.x;
-    const int c = tid / kG, g = tid % kG;
+    const int c = tid / LPC, g = tid % LPC;
     const int d0 = blockIdx.x * kCh;
     const int b = blockIdx.y;
+    const int chunk = blockIdx.z;
     const int d = d0 + c;
     const bool dvalid = d < p.dim;
-    const int64_t L = p.seqlen;
-    const int nst = (int)((L + kT - 1) / kT);
+    const int64_t t_begin = (int64_t)chunk * p.chunk;
+    const int64_t t_end = t_begin + p.chunk < p.seqlen ? t_begin + p.chunk : p.seqlen;
+    const int64_t len = t_end - t_begin;
+    const int ntiles = (int)((len + kT - 1) / kT);
 
+    // initial state: h0 for the first chunk, the carried state for the others (pass 2),
+    // zero in pass 1
+    const float* hinit = nullptr;
+    if constexpr (MODE == kFull) {
+        if (chunk == 0)
+            hinit = p.h0 ? p.h0 + ((int64_t)b * p.dim) * N : nullptr;
+        else
+            hinit = p.carry + ((int64_t)(chunk - 1) * gridDim.y + b) * p.dim * N;
+    }
     f2 A2[P], h[P];
 #pragma unroll
     for (int k = 0; k < P; ++k) {
@@ -129,28 +157,46 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         if (dvalid) {
             a0 = p.A[(int64_t)d * N + n] * kLog2e;
             a1 = p.A[(int64_t)d * N + n + 1] * kLog2e;
-            if (p.h0) {
-                h0v = p.h0[((int64_t)b * p.dim + d) * N + n];
-                h1v = p.h0[((int64_t)b * p.dim + d) * N + n + 1];
+            if (hinit) {
+                h0v = hinit[(int64_t)d * N + n];
+                h1v = hinit[(int64_t)d * N + n + 1];
             }
         }
         A2[k] = pk(a0, a1);
         h[k] = pk(h0v, h1v);
     }
-    const float bias = (dvalid && p.bias) ? p.bias[d] : 0.f;
-    const float Dd = (DSKIP && dvalid) ? p.D[d] : 0.f;
+
+    // producer role: thread handles channel pair cp (fixed) and rows r0, r0 + kRowStep, ...
+    constexpr int kPairs = kCh / 2;
+    constexpr int kRowStep = kThreads / kPairs;
+    const int cp = tid % kPairs;
+    const int r0 = tid / kPairs;
+    float pb0 = 0.f, pb1 = 0.f, pD0 = 0.f, pD1 = 0.f;
+    {
+        const int e0 = d0 + 2 * cp, e1 = e0 + 1;
+        if (p.bias) {
+            pb0 = e0 < p.dim ? p.bias[e0] : 0.f;
+            pb1 = e1 < p.dim ? p.bias[e1] : 0.f;
+        }
+        if (DSKIP) {
+            pD0 = e0 < p.dim ? p.D[e0] : 0.f;
+            pD1 = e1 < p.dim ? p.D[e1] : 0.f;
+        }
+    }
+    float dtsum = 0.f;   // pass 1: sum of dt over the chunk (lane 0 of each channel)
 
     auto stage_ptr = [&](int buf) { return smem + Lay::kRing + buf * Lay::kStageStride; };
     auto issue = [&](int s) {
         const int buf = s % kStages;
         unsigned char* st = stage_ptr(buf);
-        mbar_arrive_expect_tx(&bars[buf], Lay::kStageBytes - (GATE ? 0 : Lay::kTileX));
-        const int t0 = s * kT;
+        constexpr unsigned kBytes = Lay::kStageBytes - (kGate ? 0 : Lay::kTileX) - (kReadout ? 0 : Lay::kTileB);
+        mbar_arrive_expect_tx(&bars[buf], kBytes);
+        const int t0 = (int)(t_begin + (int64_t)s * kT);
         tma_load_3d(st, &mx, d0, t0, b, &bars[buf]);
         tma_load_3d(st + Lay::kTileX, &md, d0, t0, b, &bars[buf]);
-        if constexpr (GATE) tma_load_3d(st + 2 * Lay::kTileX, &mz, d0, t0, b, &bars[buf]);
+        if constexpr (kGate) tma_load_3d(st + 2 * Lay::kTileX, &mz, d0, t0, b, &bars[buf]);
         tma_load_3d(st + 3 * Lay::kTileX, &mB, 0, t0, b, &bars[buf]);
-        tma_load_3d(st + 3 * Lay::kTileX + Lay::kTileB, &mC, 0, t0, b, &bars[buf]);
+        if constexpr (kReadout) tma_load_3d(st + 3 * Lay::kTileX + Lay::kTileB, &mC, 0, t0, b, &bars[buf]);
     };
 
     if (tid == 0) {
@@ -158,28 +204,61 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         fence_mbar_init();
         prefetch_tensormap(&mx);
         prefetch_tensormap(&mB);
-        for (int s = p.skip_first_load ? 1 : 0; s < kStages && s < nst; ++s) issue(s);
+        for (int s = p.skip_first_load ? 1 : 0; s < kStages && s < ntiles; ++s) issue(s);
     }
     __syncthreads();
 
     bool failed = false;
-    for (int s = 0; s < nst; ++s) {
+    for (int s = 0; s < ntiles; ++s) {
         const int buf = s % kStages;
+        const int rem = (int)(len - (int64_t)s * kT);
+        const int tcount = rem < kT ? rem : kT;
         const bool ok = mbar_wait_bounded(&bars[buf], (s / kStages) & 1, p.status);
         if (__syncthreads_or(!ok)) {
+            // give up on this tile; before leaving, wait (bounded) for the later tiles
+            // already issued so that no copy still targets this CTA's shared memory
+            if (tid == 0)
+                for (int s2 = s + 1; s2 < s + kStages && s2 < ntiles; ++s2)
+                    mbar_wait_bounded(&bars[s2 % kStages], (s2 / kStages) & 1, p.status);
             failed = true;
             break;
         }
-        unsigned char* st = stage_ptr(buf);
-        const void* xs = st;
-        const void* ds = st + Lay::kTileX;
-        const void* zs = st + 2 * Lay::kTileX;
-        const float* Bf;
-        const float* Cf;
+        const unsigned char* st = stage_ptr(buf);
+
+        // ---------------- producer phase
+#pragma unroll
+        for (int r = r0; r < kT; r += kRowStep) {
+            const int idx = r * kCh + 2 * cp;
+            float x0, x1, v0, v1;
+            ld_pair<BF16>(st, idx, x0, x1);
+            ld_pair<BF16>(st + Lay::kTileX, idx, v0, v1);
+            v0 += pb0;
+            v1 += pb1;
+            if constexpr (SOFTPLUS) {
+                v0 = softplus_fast(v0);
+                v1 = softplus_fast(v1);
+            }
+            const bool tv = r < tcount;
+            const float dt0 = tv ? v0 : 0.f, dt1 = tv ? v1 : 0.f;
+            const float u0 = dt0 * x0, u1 = dt1 * x1;
+            sc[r * kCh + 2 * cp] = make_float4(dt0, dt0, u0, u0);
+            sc[r * kCh + 2 * cp + 1] = make_float4(dt1, dt1, u1, u1);
+            if constexpr (kReadout) {
+                float g0 = 1.f, g1 = 1.f;
+                if constexpr (kGate) {
+                    float z0, z1;
+                    ld_pair<BF16>(st + 2 * Lay::kTileX, idx, z0, z1);
+                    g0 = silu_fast(z0);
+                    g1 = silu_fast(z1);
+                }
+                *reinterpret_cast<float4*>(&eg[r * kCh + 2 * cp]) =
+                    make_float4(DSKIP ? pD0 * x0 : 0.f, g0, DSKIP ? pD1 * x1 : 0.f, g1);
+            }
+        }
         if constexpr (BF16) {
-            float* bcf = reinterpret_cast<float*>(smem + Lay::kBCf);
-            const uint4* src = reinterpret_cast<const uint4*>(st + 3 * Lay::kTileX);   // B then C, bf16
-            constexpr int kChunks = 2 * kT * N / 8;
+            // B then C: kReadout ? 2 : 1 tiles of kT * N bf16, widened to fp32
+            const uint4* src = reinterpret_cast<const uint4*>(st + 3 * Lay::kTileX);
+            constexpr int kChunks = (kReadout ? 2 : 1) * kT * N / 8;
 #pragma unroll
             for (int i = tid; i < kChunks; i += kThreads) {
                 const uint4 v = src[i];
@@ -189,91 +268,153 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
                 dst[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u),
                                      __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
             }
-            Bf = bcf;
-            Cf = bcf + kT * N;
         } else {
-            Bf = reinterpret_cast<const float*>(st + 3 * Lay::kTileX);
-            Cf = reinterpret_cast<const float*>(st + 3 * Lay::kTileX + Lay::kTileB);
+            const float4* src = reinterpret_cast<const float4*>(st + 3 * Lay::kTileX);
+            constexpr int kChunks = (kReadout ? 2 : 1) * kT * N / 4;
+#pragma unroll
+            for (int i = tid; i < kChunks; i += kThreads) reinterpret_cast<float4*>(bcf)[i] = src[i];
         }
         unsigned char* ys = smem + Lay::kY + (s & 1) * Lay::kYStride;
-        if (s >= 2 && tid == 0) tma_store_wait_read<1>();
+        if (kReadout && s >= 2 && tid == 0) tma_store_wait_read<1>();   // the store of tile s-2 read ys
         __syncthreads();
-        const int64_t rem = L - (int64_t)s * kT;
-        const int tcount = rem < kT ? (int)rem : kT;
-        const int ngrp = (tcount + kG - 1) / kG;
+        // the ring slot has been consumed: refill it
+        if (tid == 0 && s + kStages < ntiles) issue(s + kStages);
 
-        Scal cur = scalars<BF16, GATE, SOFTPLUS>(xs, ds, zs, g, c, bias, g < tcount);
-#pragma unroll 2
-        for (int grp = 0; grp < kT / kG; ++grp) {
-            if (grp >= ngrp) break;
-            // the next group's scalars: independent of the state, overlaps the updates below
-            const int jn = (grp + 1) * kG + g;
-            Scal nxt = scalars<BF16, GATE, SOFTPLUS>(xs, ds, zs, jn < kT ? jn : g, c, bias, jn < tcount);
-
-            float acc[kG];
+        // ---------------- update phase
+        const float* Bf = bcf;
+        const float* Cf = bcf + kT * N;
+        float yout[kT / LPC];   // the steps this lane finishes; stored after the loop so that no
+                                // shared-memory store sits between the loads of later steps
+        // The state-independent work of a group of LPC steps (A_bar, u B, C) is done one group
+        // ahead of the dependent state updates, so SFU and shared-memory latency overlap them.
+        f2 ab[2][LPC][P], vv[2][LPC][P], cc[2][LPC][P];
+        auto prepare = [&](int grp, int slot) {
 #pragma unroll
-            for (int q = 0; q < kG; ++q) {
-                const float dtq = __shfl_sync(0xffffffffu, cur.dt, q, kG);
-                const float uq = __shfl_sync(0xffffffffu, cur.u, q, kG);
-                const f2 dt2 = pk(dtq, dtq), u2 = pk(uq, uq);
-                const float* Brow = Bf + (grp * kG + q) * N + g * S;
-                const float* Crow = Cf + (grp * kG + q) * N + g * S;
-                f2 a2 = pk(0.f, 0.f);
+            for (int q = 0; q < LPC; ++q) {
+                const int t = grp * LPC + q;
+                f2 dt2, u2;
+                lds_2xf2(reinterpret_cast<const float*>(&sc[t * kCh + c]), dt2, u2);
+                if constexpr (MODE == kPass1) {
+                    if (g == 0) {
+                        float lo, hi;
+                        upk(dt2, lo, hi);
+                        dtsum += lo;
+                    }
+                }
+                const float* Brow = Bf + t * N + g * S;
+                const float* Crow = Cf + t * N + g * S;
 #pragma unroll
                 for (int k = 0; k < P; k += 2) {
-                    f2 b01, b23, c01, c23;
+                    f2 b01, b23;
                     lds_2xf2(Brow + 2 * k, b01, b23);
-                    lds_2xf2(Crow + 2 * k, c01, c23);
                     float e0, e1, e2, e3;
                     upk(mul2(dt2, A2[k]), e0, e1);
                     upk(mul2(dt2, A2[k + 1]), e2, e3);
-                    const f2 ab01 = pk(ex2_approx(e0), ex2_approx(e1));
-                    const f2 ab23 = pk(ex2_approx(e2), ex2_approx(e3));
-                    h[k] = fma2(ab01, h[k], mul2(u2, b01));
-                    h[k + 1] = fma2(ab23, h[k + 1], mul2(u2, b23));
-                    a2 = fma2(c01, h[k], a2);
-                    a2 = fma2(c23, h[k + 1], a2);
+                    ab[slot][q][k] = pk(ex2_approx(e0), ex2_approx(e1));
+                    ab[slot][q][k + 1] = pk(ex2_approx(e2), ex2_approx(e3));
+                    vv[slot][q][k] = mul2(u2, b01);
+                    vv[slot][q][k + 1] = mul2(u2, b23);
+                    if constexpr (kReadout) lds_2xf2(Crow + 2 * k, cc[slot][q][k], cc[slot][q][k + 1]);
                 }
-                float lo, hi;
-                upk(a2, lo, hi);
-                acc[q] = lo + hi;
             }
-            // reduce-scatter: lane g ends with the full sum of step g
-            const bool hi2 = (g & 2) != 0;
-            const float ra = (hi2 ? acc[2] : acc[0]) + __shfl_xor_sync(0xffffffffu, hi2 ? acc[0] : acc[2], 2);
-            const float rb = (hi2 ? acc[3] : acc[1]) + __shfl_xor_sync(0xffffffffu, hi2 ? acc[1] : acc[3], 2);
-            const bool hi1 = (g & 1) != 0;
-            const float tot = (hi1 ? rb : ra) + __shfl_xor_sync(0xffffffffu, hi1 ? ra : rb, 1);
-            const int jj = grp * kG + g;
-            if (jj < tcount) {
-                float out = DSKIP ? fmaf(Dd, cur.xr, tot) : tot;
-                if constexpr (GATE) out *= cur.gate;
-                if constexpr (BF16)
-                    reinterpret_cast<__nv_bfloat16*>(ys)[jj * kCh + c] = __float2bfloat16_rn(out);
-                else
-                    reinterpret_cast<float*>(ys)[jj * kCh + c] = out;
+        };
+        prepare(0, 0);
+#pragma unroll
+        for (int grp = 0; grp < kT / LPC; ++grp) {
+            const int cur = grp & 1;
+            if (grp + 1 < kT / LPC) prepare(grp + 1, cur ^ 1);
+            float acc[LPC];
+#pragma unroll
+            for (int q = 0; q < LPC; ++q) {
+                f2 a2 = pk(0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < P; ++k) {
+                    h[k] = fma2(ab[cur][q][k], h[k], vv[cur][q][k]);
+                    if constexpr (kReadout) a2 = fma2(cc[cur][q][k], h[k], a2);
+                }
+                if constexpr (kReadout) {
+                    float lo, hi;
+                    upk(a2, lo, hi);
+                    acc[q] = lo + hi;
+                }
             }
-            cur = nxt;
+            if constexpr (kReadout) {
+                // reduce-scatter over the LPC lanes of the channel: lane g ends with step g's sum
+                float tot;
+                if constexpr (LPC == 4) {
+                    const bool hi2 = (g & 2) != 0;
+                    const float ra = (hi2 ? acc[2] : acc[0]) + __shfl_xor_sync(0xffffffffu, hi2 ? acc[0] : acc[2], 2);
+                    const float rb = (hi2 ? acc[3] : acc[1]) + __shfl_xor_sync(0xffffffffu, hi2 ? acc[1] : acc[3], 2);
+                    const bool hi1 = (g & 1) != 0;
+                    tot = (hi1 ? rb : ra) + __shfl_xor_sync(0xffffffffu, hi1 ? ra : rb, 1);
+                } else {
+                    const bool hi1 = (g & 1) != 0;
+                    tot = (hi1 ? acc[1] : acc[0]) + __shfl_xor_sync(0xffffffffu, hi1 ? acc[0] : acc[1], 1);
+                }
+                const int jj = grp * LPC + g;
+                const float2 e = eg[jj * kCh + c];
+                yout[grp] = (tot + e.x) * e.y;
+            }
         }
-        fence_proxy_async_smem();
+        if constexpr (kReadout) {
+#pragma unroll
+            for (int grp = 0; grp < kT / LPC; ++grp) {
+                const int jj = grp * LPC + g;
+                if constexpr (BF16)
+                    reinterpret_cast<__nv_bfloat16*>(ys)[jj * kCh + c] = __float2bfloat16_rn(yout[grp]);
+                else
+                    reinterpret_cast<float*>(ys)[jj * kCh + c] = yout[grp];
+            }
+        }
+        if constexpr (kReadout) fence_proxy_async_smem();
         __syncthreads();
-        if (tid == 0) {
-            tma_store_3d(&my, d0, s * kT, b, ys);
+        if (kReadout && tid == 0) {
+            tma_store_3d(&my, d0, (int)(t_begin + (int64_t)s * kT), b, ys);
             tma_store_commit();
-            if (s + kStages < nst) issue(s + kStages);
         }
     }
-    if (tid == 0) tma_store_wait_all();
+    if (kReadout && tid == 0) tma_store_wait_all();
     if (failed) return;
-    if (dvalid && p.h_last) {
+    if (!dvalid) return;
+    if constexpr (MODE == kFull) {
+        if (p.h_last && chunk == (int)gridDim.z - 1) {
+            float* out = p.h_last + ((int64_t)b * p.dim + d) * N;
+#pragma unroll
+            for (int k = 0; k < P; ++k) {
+                float lo, hi;
+                upk(h[k], lo, hi);
+                *reinterpret_cast<float2*>(out + g * S + 2 * k) = make_float2(lo, hi);
+            }
+        }
+    } else {
+        float* out = p.carry + (((int64_t)chunk * gridDim.y + b) * p.dim + d) * N;
 #pragma unroll
         for (int k = 0; k < P; ++k) {
             float lo, hi;
             upk(h[k], lo, hi);
-            const int n = g * S + 2 * k;
-            p.h_last[((int64_t)b * p.dim + d) * N + n] = lo;
-            p.h_last[((int64_t)b * p.dim + d) * N + n + 1] = hi;
+            *reinterpret_cast<float2*>(out + g * S + 2 * k) = make_float2(lo, hi);
         }
+        if (g == 0) p.sumdt[((int64_t)chunk * gridDim.y + b) * p.dim + d] = dtsum;
+    }
+}
+
+// Chunk carry: one thread per (b, d, n) walks the chunks in order,
+//   H_0 = h0,  H_{c+1} = exp(A[d, n] * sumdt_c) * H_c + local_c,
+// and stores H_{c+1} over local_c (the initial state of chunk c + 1).
+__global__ void scan_carry_kernel(float* carry, const float* sumdt, const float* A, const float* h0,
+                                  int64_t batch, int64_t dim, int N, int nsteps) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t total = batch * dim * N;
+    if (i >= total) return;
+    const int64_t bd = i / N;
+    const int n = (int)(i % N);
+    const int64_t d = bd % dim;
+    const float a = A[d * N + n];
+    float H = h0 ? h0[i] : 0.f;
+    for (int c = 0; c < nsteps; ++c) {
+        const int64_t o = (int64_t)c * total + i;
+        H = fmaf(expf(a * sumdt[(int64_t)c * batch * dim + bd]), H, carry[o]);
+        carry[o] = H;
     }
 }
 
@@ -312,34 +453,67 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t inner, int64_
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-template <int N, bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS>
-cudaError_t launch_t(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, cudaStream_t st) {
+// Lanes per channel: 2 for N = 16 (8 states a lane), 4 above.
+template <int N>
+constexpr int lanes_per_channel() { return N == 16 ? 2 : 4; }
+
+template <int N, bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS, int MODE, int LPC = lanes_per_channel<N>()>
+cudaError_t launch_t(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz, cudaStream_t st) {
     using Lay = Layout<N, BF16>;
-    auto kern = scan_fast_kernel<N, BF16, GATE, DSKIP, SOFTPLUS>;
+    if constexpr (N == 16 && LPC == 2) {
+        static const bool four = [] {
+            const char* e = getenv("SSMSCAN_N16_LANES");
+            return e && e[0] == '4';
+        }();
+        if (four) return launch_t<N, BF16, GATE, DSKIP, SOFTPLUS, MODE, 4>(maps, fp, a, nz, st);
+    }
+    auto kern = scan_fast_kernel<N, BF16, LPC, GATE, DSKIP, SOFTPLUS, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kTotal);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((a.dim + kCh - 1) / kCh), (unsigned)a.batch);
-    kern<<<grid, kThreads, Lay::kTotal, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], fp);
+    dim3 grid((unsigned)((a.dim + kCh - 1) / kCh), (unsigned)a.batch, (unsigned)nz);
+    kern<<<grid, kCh * LPC, Lay::kTotal, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], fp);
     note_launches(1);
     return cudaGetLastError();
 }
 
-template <int N, bool BF16>
-cudaError_t dispatch_flags(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, cudaStream_t st) {
+template <int N, bool BF16, int MODE>
+cudaError_t dispatch_flags(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz, cudaStream_t st) {
     const bool gate = a.z != nullptr, dskip = a.D != nullptr, sp = a.softplus != 0;
+    if constexpr (MODE == kPass1) {
+        // pass 1 reads neither z nor D
+        return sp ? launch_t<N, BF16, false, false, true, MODE>(maps, fp, a, nz, st)
+                  : launch_t<N, BF16, false, false, false, MODE>(maps, fp, a, nz, st);
+    } else {
 #define SSM_FAST_CASE(G_, D_, S_) \
-    if (gate == G_ && dskip == D_ && sp == S_) return launch_t<N, BF16, G_, D_, S_>(maps, fp, a, st);
-    SSM_FAST_CASE(true, true, true)
-    SSM_FAST_CASE(true, true, false)
-    SSM_FAST_CASE(true, false, true)
-    SSM_FAST_CASE(true, false, false)
-    SSM_FAST_CASE(false, true, true)
-    SSM_FAST_CASE(false, true, false)
-    SSM_FAST_CASE(false, false, true)
-    SSM_FAST_CASE(false, false, false)
+    if (gate == G_ && dskip == D_ && sp == S_) return launch_t<N, BF16, G_, D_, S_, MODE>(maps, fp, a, nz, st);
+        SSM_FAST_CASE(true, true, true)
+        SSM_FAST_CASE(true, true, false)
+        SSM_FAST_CASE(true, false, true)
+        SSM_FAST_CASE(true, false, false)
+        SSM_FAST_CASE(false, true, true)
+        SSM_FAST_CASE(false, true, false)
+        SSM_FAST_CASE(false, false, true)
+        SSM_FAST_CASE(false, false, false)
 #undef SSM_FAST_CASE
+    }
     return cudaErrorInvalidValue;
 }
+
+template <int MODE>
+cudaError_t dispatch(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz, cudaStream_t st) {
+    const bool bf = a.io_bf16 != 0;
+    switch (a.dstate) {
+        case 16: return bf ? dispatch_flags<16, true, MODE>(maps, fp, a, nz, st)
+                           : dispatch_flags<16, false, MODE>(maps, fp, a, nz, st);
+        case 32: return bf ? dispatch_flags<32, true, MODE>(maps, fp, a, nz, st)
+                           : dispatch_flags<32, false, MODE>(maps, fp, a, nz, st);
+        case 64: return bf ? dispatch_flags<64, true, MODE>(maps, fp, a, nz, st)
+                           : dispatch_flags<64, false, MODE>(maps, fp, a, nz, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+constexpr int64_t kMinChunk = 512;    // shortest chunk the automatic split uses
 
 }  // namespace
 
@@ -347,7 +521,7 @@ bool scan_fast_supported(const ScanArgs& a) {
     const int N = a.dstate;
     if (N != 16 && N != 32 && N != 64) return false;
     if (a.reverse || a.zoh) return false;
-    if (a.batch > 65535 || a.dim > (int64_t)1 << 30 || a.seqlen > ((int64_t)1 << 31) - kT) return false;
+    if (a.batch > 65535 || a.dim > (int64_t)1 << 30 || a.seqlen > ((int64_t)1 << 31) - 2 * kT) return false;
     if (!encode_fn()) return false;
     const int64_t esz = a.io_bf16 ? 2 : 4;
     auto act_ok = [&](const void* ptr, const int64_t* s) {
@@ -367,6 +541,33 @@ bool scan_fast_supported(const ScanArgs& a) {
            bc_ok(a.B, a.Bs) && bc_ok(a.C, a.Cs);
 }
 
+int64_t scan_fast_chunk(const ScanArgs& a) {
+    const int64_t L = a.seqlen;
+    int64_t q;
+    if (a.chunk_len > 0) {
+        q = a.chunk_len;
+    } else {
+        // split only when the channel tiles leave the SMs short of work
+        const int64_t tiles = a.batch * ((a.dim + kCh - 1) / kCh);
+        const int64_t want = 8 * 148;
+        if (tiles >= 2 * 148 || L < 2 * kMinChunk) return ((L + kT - 1) / kT) * kT;
+        int64_t nch = (want + tiles - 1) / tiles;
+        q = (L + nch - 1) / nch;
+        if (q < kMinChunk) q = kMinChunk;
+    }
+    q = ((q + kT - 1) / kT) * kT;
+    if (q >= L) q = ((L + kT - 1) / kT) * kT;
+    return q;
+}
+
+size_t scan_fast_workspace_bytes(const ScanArgs& a) {
+    if (a.seqlen == 0) return 0;
+    const int64_t q = scan_fast_chunk(a);
+    const int64_t nch = (a.seqlen + q - 1) / q;
+    if (nch <= 1) return 0;
+    return (size_t)((nch - 1) * a.batch * a.dim * (a.dstate + 1)) * sizeof(float);
+}
+
 cudaError_t launch_scan_fast(const ScanArgs& a, cudaStream_t st) {
     CUtensorMap maps[6];
     const bool bf = a.io_bf16 != 0;
@@ -379,15 +580,25 @@ cudaError_t launch_scan_fast(const ScanArgs& a, cudaStream_t st) {
         !make_map(&maps[4], a.C, bf, a.dstate, a.seqlen, a.batch, a.Cs[1], a.Cs[0], a.dstate) ||
         !make_map(&maps[5], a.y, bf, a.dim, a.seqlen, a.batch, a.ys[1], a.ys[0], kCh))
         return cudaErrorInvalidValue;
-    FastParams fp{a.seqlen, (int)a.dim, a.A, a.D, a.bias, a.h0, a.h_last, device_status_ptr(),
-                  (a.debug_flags & SSM_DEBUG_SKIP_FIRST_LOAD) ? 1 : 0};
+    const int64_t q = scan_fast_chunk(a);
+    const int nch = (int)((a.seqlen + q - 1) / q);
+    FastParams fp{a.seqlen, q, (int)a.dim, nch, a.A, a.D, a.bias, a.h0, a.h_last, nullptr, nullptr,
+                  device_status_ptr(), (a.debug_flags & SSM_DEBUG_SKIP_FIRST_LOAD) ? 1 : 0};
     if (!fp.status) return cudaErrorInvalidValue;
-    switch (a.dstate) {
-        case 16: return bf ? dispatch_flags<16, true>(maps, fp, a, st) : dispatch_flags<16, false>(maps, fp, a, st);
-        case 32: return bf ? dispatch_flags<32, true>(maps, fp, a, st) : dispatch_flags<32, false>(maps, fp, a, st);
-        case 64: return bf ? dispatch_flags<64, true>(maps, fp, a, st) : dispatch_flags<64, false>(maps, fp, a, st);
+    if (nch > 1) {
+        const size_t carry_floats = (size_t)((nch - 1) * a.batch * a.dim * a.dstate);
+        fp.carry = static_cast<float*>(a.workspace);
+        fp.sumdt = fp.carry + carry_floats;
+        cudaError_t e = dispatch<kPass1>(maps, fp, a, nch - 1, st);
+        if (e != cudaSuccess) return e;
+        const int64_t total = a.batch * a.dim * a.dstate;
+        scan_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(fp.carry, fp.sumdt, a.A, a.h0, a.batch,
+                                                                          a.dim, a.dstate, nch - 1);
+        note_launches(1);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
-    return cudaErrorInvalidValue;
+    return dispatch<kFull>(maps, fp, a, nch, st);
 }
 
 }  // namespace ssm

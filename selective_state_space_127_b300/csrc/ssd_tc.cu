@@ -1,0 +1,485 @@
+// Mamba-2 SSD chunked scan on the fifth-generation tensor cores (tcgen05), for bf16 I/O with
+// head dimension P = 64 and state size N = 128.
+//
+// One CTA (128 threads) per (batch, head) walks the sequence in blocks of Q = 128 steps;
+// the N x P state S stays on chip (fp32 registers, thread n holding row n, plus a bf16 copy
+// in shared memory as an MMA operand). Per block, with cum_t the inclusive cumulative sum of
+// dt A_h inside the block (the decay from the block start to step t):
+//
+//   G      = C B^T                                  (Q x Q, K = N)      tcgen05, TMEM
+//   M[t,s] = G[t,s] exp(cum_t - cum_s) dt_s, s <= t; 0 above the diagonal
+//   Y      = M X                                    (Q x P, K = Q)      tcgen05, A from TMEM
+//   Yoff   = C S_prev                               (Q x P, K = N)      tcgen05
+//   y_t    = Y_t + exp(cum_t) Yoff_t  (+ D x_t) (* silu z_t)
+//   S      = exp(cum_last) S_prev + B^T (w o X),    w_s = exp(cum_last - cum_s) dt_s
+//                                                   (N x P, K = Q)      tcgen05
+//
+// which is the block decomposition of the semiseparable matrix of the recurrence
+// S_t = exp(dt_t A_h) S_{t-1} + dt_t B_t x_t^T, y_t = S_t^T C_t: diagonal blocks as masked
+// matrix products, the hand-off between blocks through the state (a rank-N product).
+// A chunk of Q' = 128 k steps (the chunk length the caller asks for) is computed as k such
+// blocks; the result does not depend on the chunk length beyond rounding.
+//
+// Data movement: TMA (4-D maps, 128-byte swizzle) brings the C and B blocks (128 x 128) and
+// the x block (128 x 64) into shared memory in the layouts the MMAs read directly (C and B
+// K-major for G and Yoff; B as the MN-major A operand of the state product; x MN-major as
+// the B operand); the y block leaves by TMA store from the x buffer. Tensor memory holds G
+// (128 columns, overwritten in place by the bf16 M as the A operand of M X, then by the state
+// product), Y (64) and Yoff (64): 256 columns, so two CTAs fit on an SM.
+//
+// Pages: "Mamba-2 / Structured State Space Duality" (abeam) "基本アイデア" (SSM as a
+// semiseparable matrix; diagonal blocks by ordinary matrix products, off-diagonal blocks by a
+// low-rank hand-off of the state) and "線形形式と二次形式を使い分ける"; "Mamba/SSM complete
+// guide" section 6 "SSD演算の概念" (intra-chunk matrix products on tensor cores, inter-chunk
+// state recurrence) and `Mamba2Block` (one A per head, B and C shared by the heads of a group).
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+#include "tma.cuh"
+
+namespace ssm {
+namespace {
+
+constexpr int kQ = 128;          // steps per block
+constexpr int kP = 64;           // head dimension
+constexpr int kN = 128;          // state size
+constexpr int kThreads = 128;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColG = 0;    // G, then M (bf16 pairs, columns 0..63) and the state product (64..127)
+constexpr uint32_t kColM = 0;
+constexpr uint32_t kColS = 64;
+constexpr uint32_t kColY = 128;
+constexpr uint32_t kColYoff = 192;
+
+constexpr int kAtom = 16384;     // 128 rows x 128 bytes
+constexpr int kSmC = 0;
+constexpr int kSmB = 2 * kAtom;
+constexpr int kSmX = 4 * kAtom;
+constexpr int kSmS = 5 * kAtom;
+constexpr int kSmCs = 6 * kAtom;             // float [kQ]: cum_t log2(e)
+constexpr int kSmDt = kSmCs + kQ * 4;        // float [kQ]: dt_t
+constexpr int kSmRed = kSmDt + kQ * 4;       // float [4]: warp totals of the scan
+constexpr int kSmBar = kSmRed + 64;          // 2 mbarriers
+constexpr int kSmTmem = kSmBar + 16;         // tensor-memory base address
+constexpr int kSmemUsed = kSmTmem + 16;
+constexpr int kSmemBytes = kSmemUsed + 1024; // room to align the base to 1024 bytes
+
+constexpr uint32_t kIdescG = tc::idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescYoff = tc::idesc_bf16(128, 64, false, true);
+constexpr uint32_t kIdescY = tc::idesc_bf16(128, 64, false, true);
+constexpr uint32_t kIdescS = tc::idesc_bf16(128, 64, true, true);
+
+struct TcParams {
+    int64_t seqlen;
+    int nheads;
+    int heads_per_group;
+    int nblocks;
+    int softplus;
+    const void* x;         // (b, L, H, P) bf16, for the D skip
+    const void* delta;     // (b, L, H) bf16
+    const float* A;
+    const float* D;
+    const void* z;         // (b, L, H, P) bf16 or NULL
+    const float* bias;
+    const float* h0;       // (b, H, N, P) fp32 or NULL
+    float* h_last;         // (b, H, N, P) fp32 or NULL
+    unsigned* status;
+};
+
+__device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
+    return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                             const void* src) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(src))
+                 : "memory");
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__global__ void __launch_bounds__(kThreads)
+ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUtensorMap mB,
+              const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap mY, const TcParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                         ~static_cast<uintptr_t>(1023));
+    unsigned char* sC = sm + kSmC;
+    unsigned char* sB = sm + kSmB;
+    unsigned char* sX = sm + kSmX;
+    unsigned char* sS = sm + kSmS;
+    float* cs = reinterpret_cast<float*>(sm + kSmCs);
+    float* dts = reinterpret_cast<float*>(sm + kSmDt);
+    float* red = reinterpret_cast<float*>(sm + kSmRed);
+    uint64_t* bar_load = reinterpret_cast<uint64_t*>(sm + kSmBar);
+    uint64_t* bar_mma = bar_load + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kSmTmem);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int grp = h / p.heads_per_group;
+    const int64_t L = p.seqlen;
+    const int H = p.nheads;
+
+    if (warp == 0) tc::tmem_alloc(tslot, kTmemCols);
+    if (tid == 0) {
+        mbar_init(bar_load, 1);
+        mbar_init(bar_mma, 1);
+        fence_mbar_init();
+        prefetch_tensormap(&mX);
+        prefetch_tensormap(&mB);
+        prefetch_tensormap(&mC);
+        prefetch_tensormap(&mY);
+    }
+
+    // the state: thread n holds row n (P fp32 values); its bf16 copy is the B operand of C S
+    float S[kP];
+    {
+        const float* src = p.h0 ? p.h0 + (((int64_t)b * H + h) * kN + tid) * kP : nullptr;
+#pragma unroll
+        for (int i = 0; i < kP; i += 4) {
+            const float4 v = src ? *reinterpret_cast<const float4*>(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            S[i] = v.x;
+            S[i + 1] = v.y;
+            S[i + 2] = v.z;
+            S[i + 3] = v.w;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint4 v;
+            v.x = tc::pack_bf16(S[8 * j], S[8 * j + 1]);
+            v.y = tc::pack_bf16(S[8 * j + 2], S[8 * j + 3]);
+            v.z = tc::pack_bf16(S[8 * j + 4], S[8 * j + 5]);
+            v.w = tc::pack_bf16(S[8 * j + 6], S[8 * j + 7]);
+            *reinterpret_cast<uint4*>(sS + sw128(tid, j)) = v;
+        }
+    }
+    fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tslot;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+
+    const float Ah = p.A[h];
+    const float bias = p.bias ? p.bias[h] : 0.f;
+    const float Dh = p.D ? p.D[h] : 0.f;
+    const uint32_t aC = smem_u32(sC), aB = smem_u32(sB), aX = smem_u32(sX), aS = smem_u32(sS);
+    const __nv_bfloat16* delta = static_cast<const __nv_bfloat16*>(p.delta);
+
+    unsigned ph_load = 0, ph_mma = 0;
+    bool failed = false;
+    for (int j = 0; j < p.nblocks; ++j) {
+        const int t0 = j * kQ;
+        if (tid == 0) {
+            if (j > 0) tma_store_wait_read<0>();   // the previous y block has left sX
+            mbar_arrive_expect_tx(bar_load, 4 * kAtom + kAtom);
+            tma_load_4d(sC, &mC, 0, grp, t0, b, bar_load);
+            tma_load_4d(sC + kAtom, &mC, 64, grp, t0, b, bar_load);
+            tma_load_4d(sB, &mB, 0, grp, t0, b, bar_load);
+            tma_load_4d(sB + kAtom, &mB, 64, grp, t0, b, bar_load);
+            tma_load_4d(sX, &mX, 0, h, t0, b, bar_load);
+        }
+        // dt_t and the inclusive cumulative sum of dt A_h over the block (row t = tid)
+        const int64_t t = t0 + tid;
+        float dt = 0.f;
+        if (t < L) {
+            float v = __bfloat162float(delta[((int64_t)b * L + t) * H + h]) + bias;
+            dt = p.softplus ? softplus_accurate(v) : v;
+        }
+        float cum = dt * Ah;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, cum, o);
+            if (lane >= o) cum += n;
+        }
+        if (lane == 31) red[warp] = cum;
+        __syncthreads();
+        float before = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+            if (w < warp) before += red[w];
+        cum += before;
+        const float cum_last = red[0] + red[1] + red[2] + red[3];
+        const float cs_t = cum * kLog2e;
+        cs[tid] = cs_t;
+        dts[tid] = dt;
+        const float w_t = ex2_approx((cum_last - cum) * kLog2e) * dt;
+        const float e_t = ex2_approx(cs_t);
+        const float e_last = ex2_approx(cum_last * kLog2e);
+
+        const bool ok = mbar_wait_bounded(bar_load, ph_load, p.status);
+        ph_load ^= 1;
+        if (__syncthreads_or(!ok)) {
+            failed = true;
+            break;
+        }
+        // G = C B^T and Yoff = C S_prev
+        if (tid == 0) {
+            tc::fence_after_sync();
+#pragma unroll
+            for (int k = 0; k < kN / 16; ++k) {
+                const uint32_t off = (k / 4) * kAtom + (k % 4) * 32;
+                tc::mma_ss(tmem + kColG, tc::sdesc_sw128(aC + off, 16, 1024), tc::sdesc_sw128(aB + off, 16, 1024),
+                           kIdescG, k > 0);
+            }
+#pragma unroll
+            for (int k = 0; k < kN / 16; ++k) {
+                const uint32_t off = (k / 4) * kAtom + (k % 4) * 32;
+                tc::mma_ss(tmem + kColYoff, tc::sdesc_sw128(aC + off, 16, 1024),
+                           tc::sdesc_sw128(aS + k * 2048, kAtom, 1024), kIdescYoff, k > 0);
+            }
+            tc::commit(bar_mma);
+        }
+        if (!mbar_wait_bounded(bar_mma, ph_mma, p.status)) failed = true;
+        ph_mma ^= 1;
+        tc::fence_after_sync();
+
+        // M[t, s] = G[t, s] exp(cum_t - cum_s) dt_s for s <= t, written in place over G as
+        // bf16 pairs (columns 16 kc .. 16 kc + 15 after columns 32 kc .. 32 kc + 31 are read)
+#pragma unroll 1
+        for (int kc = 0; kc < 4; ++kc) {
+            uint32_t packed[16];
+            if (kc <= warp) {            // warp-uniform: column blocks above the diagonal stay zero
+                uint32_t r[32];
+                tc::ld32(lane_base + kColG + 32 * kc, r);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const int s0 = 32 * kc + i;
+                    const float m0 = s0 <= tid ? __uint_as_float(r[i]) * ex2_approx(cs_t - cs[s0]) * dts[s0] : 0.f;
+                    const float m1 =
+                        s0 + 1 <= tid ? __uint_as_float(r[i + 1]) * ex2_approx(cs_t - cs[s0 + 1]) * dts[s0 + 1] : 0.f;
+                    packed[i / 2] = tc::pack_bf16(m0, m1);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) packed[i] = 0u;
+            }
+            tc::st16(lane_base + kColM + 16 * kc, packed);
+        }
+        tc::wait_st();
+        tc::fence_before_sync();
+        __syncthreads();
+        // Y = M X
+        if (tid == 0) {
+            tc::fence_after_sync();
+#pragma unroll
+            for (int k = 0; k < kQ / 16; ++k)
+                tc::mma_ts(tmem + kColY, tmem + kColM + 8 * k, tc::sdesc_sw128(aX + k * 2048, kAtom, 1024), kIdescY,
+                           k > 0);
+            tc::commit(bar_mma);
+        }
+        if (!mbar_wait_bounded(bar_mma, ph_mma, p.status)) failed = true;
+        ph_mma ^= 1;
+        tc::fence_after_sync();
+
+        // x row s (= tid) scaled in place by w_s: the B operand of the state product
+        {
+            uint4* row = reinterpret_cast<uint4*>(sX + tid * 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint4 v = row[c];
+                v.x = tc::pack_bf16(bf_lo(v.x) * w_t, bf_hi(v.x) * w_t);
+                v.y = tc::pack_bf16(bf_lo(v.y) * w_t, bf_hi(v.y) * w_t);
+                v.z = tc::pack_bf16(bf_lo(v.z) * w_t, bf_hi(v.z) * w_t);
+                v.w = tc::pack_bf16(bf_lo(v.w) * w_t, bf_hi(v.w) * w_t);
+                row[c] = v;
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        // S_acc = B^T (w o X)
+        if (tid == 0) {
+            tc::fence_after_sync();
+#pragma unroll
+            for (int k = 0; k < kQ / 16; ++k)
+                tc::mma_ss(tmem + kColS, tc::sdesc_sw128(aB + k * 2048, kAtom, 1024),
+                           tc::sdesc_sw128(aX + k * 2048, kAtom, 1024), kIdescS, k > 0);
+            tc::commit(bar_mma);
+        }
+        if (!mbar_wait_bounded(bar_mma, ph_mma, p.status)) failed = true;
+        ph_mma ^= 1;
+        tc::fence_after_sync();
+        if (__syncthreads_or(failed)) {
+            failed = true;
+            break;
+        }
+
+        // epilogue: y row t = tid into sX (free now), the state row n = tid
+        const __nv_bfloat16* xrow =
+            p.D && t < L ? static_cast<const __nv_bfloat16*>(p.x) + (((int64_t)b * L + t) * H + h) * kP : nullptr;
+        const __nv_bfloat16* zrow =
+            p.z && t < L ? static_cast<const __nv_bfloat16*>(p.z) + (((int64_t)b * L + t) * H + h) * kP : nullptr;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t ry[32], ro[32];
+            tc::ld32(lane_base + kColY + 32 * half, ry);
+            tc::ld32(lane_base + kColYoff + 32 * half, ro);
+            tc::wait_ld();
+            float yv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) yv[i] = fmaf(e_t, __uint_as_float(ro[i]), __uint_as_float(ry[i]));
+            if (xrow) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(xrow + 32 * half + i);
+                    yv[i] = fmaf(Dh, bf_lo(v.x), yv[i]);
+                    yv[i + 1] = fmaf(Dh, bf_hi(v.x), yv[i + 1]);
+                    yv[i + 2] = fmaf(Dh, bf_lo(v.y), yv[i + 2]);
+                    yv[i + 3] = fmaf(Dh, bf_hi(v.y), yv[i + 3]);
+                    yv[i + 4] = fmaf(Dh, bf_lo(v.z), yv[i + 4]);
+                    yv[i + 5] = fmaf(Dh, bf_hi(v.z), yv[i + 5]);
+                    yv[i + 6] = fmaf(Dh, bf_lo(v.w), yv[i + 6]);
+                    yv[i + 7] = fmaf(Dh, bf_hi(v.w), yv[i + 7]);
+                }
+            }
+            if (zrow) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(zrow + 32 * half + i);
+                    yv[i] *= silu_accurate(bf_lo(v.x));
+                    yv[i + 1] *= silu_accurate(bf_hi(v.x));
+                    yv[i + 2] *= silu_accurate(bf_lo(v.y));
+                    yv[i + 3] *= silu_accurate(bf_hi(v.y));
+                    yv[i + 4] *= silu_accurate(bf_lo(v.z));
+                    yv[i + 5] *= silu_accurate(bf_hi(v.z));
+                    yv[i + 6] *= silu_accurate(bf_lo(v.w));
+                    yv[i + 7] *= silu_accurate(bf_hi(v.w));
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint4 v;
+                v.x = tc::pack_bf16(yv[8 * c], yv[8 * c + 1]);
+                v.y = tc::pack_bf16(yv[8 * c + 2], yv[8 * c + 3]);
+                v.z = tc::pack_bf16(yv[8 * c + 4], yv[8 * c + 5]);
+                v.w = tc::pack_bf16(yv[8 * c + 6], yv[8 * c + 7]);
+                *reinterpret_cast<uint4*>(sX + sw128(tid, 4 * half + c)) = v;
+            }
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t rs[32];
+            tc::ld32(lane_base + kColS + 32 * half, rs);
+            tc::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) S[32 * half + i] = fmaf(e_last, S[32 * half + i], __uint_as_float(rs[i]));
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            uint4 v;
+            v.x = tc::pack_bf16(S[8 * c], S[8 * c + 1]);
+            v.y = tc::pack_bf16(S[8 * c + 2], S[8 * c + 3]);
+            v.z = tc::pack_bf16(S[8 * c + 4], S[8 * c + 5]);
+            v.w = tc::pack_bf16(S[8 * c + 6], S[8 * c + 7]);
+            *reinterpret_cast<uint4*>(sS + sw128(tid, c)) = v;
+        }
+        fence_proxy_async_smem();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tma_store_4d(&mY, 0, h, t0, b, sX);
+            tma_store_commit();
+        }
+    }
+    if (tid == 0) tma_store_wait_all();
+    if (!failed && p.h_last) {
+        float* dst = p.h_last + (((int64_t)b * H + h) * kN + tid) * kP;
+#pragma unroll
+        for (int i = 0; i < kP; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn4() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
+    return fn;
+}
+
+// 4-D bf16 map over a contiguous (d3, d2, d1, d0) tensor, box {64, 1, 128, 1}, 128-byte swizzle.
+bool make_map4(CUtensorMap* m, const void* base, int64_t d0, int64_t d1, int64_t d2, int64_t d3) {
+    auto fn = encode_fn4();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2, (cuuint64_t)d3};
+    cuuint64_t strides[3] = {(cuuint64_t)(d0 * 2), (cuuint64_t)(d0 * d1 * 2), (cuuint64_t)(d0 * d1 * d2 * 2)};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)kQ, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool al16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; }
+
+}  // namespace
+
+bool ssd_tc_supported(const SSDArgs& a) {
+    if (!a.io_bf16 || a.headdim != kP || a.dstate != kN) return false;
+    if (a.chunk % kQ != 0) return false;
+    if (a.nheads > 65535 || a.batch > 65535 || a.seqlen > ((int64_t)1 << 30)) return false;
+    if (!al16(a.x) || !al16(a.B) || !al16(a.C) || !al16(a.y)) return false;
+    if (a.z && !al16(a.z)) return false;
+    if (a.h0 && !al16(a.h0)) return false;
+    if (a.h_last && !al16(a.h_last)) return false;
+    return encode_fn4() != nullptr;
+}
+
+cudaError_t launch_ssd_tc(const SSDArgs& a, cudaStream_t st) {
+    CUtensorMap mX, mB, mC, mY;
+    if (!make_map4(&mX, a.x, kP, a.nheads, a.seqlen, a.batch) ||
+        !make_map4(&mB, a.B, kN, a.ngroups, a.seqlen, a.batch) ||
+        !make_map4(&mC, a.C, kN, a.ngroups, a.seqlen, a.batch) ||
+        !make_map4(&mY, a.y, kP, a.nheads, a.seqlen, a.batch))
+        return cudaErrorInvalidValue;
+    TcParams p;
+    p.seqlen = a.seqlen;
+    p.nheads = (int)a.nheads;
+    p.heads_per_group = (int)(a.nheads / a.ngroups);
+    p.nblocks = (int)((a.seqlen + kQ - 1) / kQ);
+    p.softplus = a.softplus;
+    p.x = a.x;
+    p.delta = a.delta;
+    p.A = a.A;
+    p.D = a.D;
+    p.z = a.z;
+    p.bias = a.bias;
+    p.h0 = a.h0;
+    p.h_last = a.h_last;
+    p.status = device_status_ptr();
+    if (!p.status) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(ssd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)a.nheads, (unsigned)a.batch);
+    ssd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mX, mB, mC, mY, p);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace ssm

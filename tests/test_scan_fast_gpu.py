@@ -78,7 +78,7 @@ def test_bf16_outputs_are_the_rounded_oracle(cuda_dev):
 def test_injected_missing_copy_times_out_and_context_survives(cuda_dev):
     """The test hook withholds the first TMA copy: the bounded wait gives up after about a
     second, the status word reads SSM_ERR_TIMEOUT, and the next call works normally."""
-    inp = _to(cuda_dev, make_scan_inputs(1, 20, 32, 16, "bf16", seed=5))
+    inp = _to(cuda_dev, make_scan_inputs(1, 16, 32, 16, "bf16", seed=5))
     assert device_status() == binding.SSM_OK
     ssm_scan_fwd(**inp, debug_flags=binding.SSM_DEBUG_SKIP_FIRST_LOAD)
     assert device_status(clear=True) == binding.SSM_ERR_TIMEOUT
@@ -93,3 +93,45 @@ def test_debug_hook_is_refused_where_it_could_leave_copies_in_flight(cuda_dev):
     with pytest.raises(binding.SSMError) as e:
         ssm_scan_fwd(**inp, debug_flags=binding.SSM_DEBUG_SKIP_FIRST_LOAD)
     assert e.value.status == binding.SSM_ERR_INVALID_ARG
+
+
+CHUNK_CASES = [
+    # b, L, D, N, dtype, chunk_len, with h0
+    (1, 1000, 32, 16, "bf16", 64, True),      # 16 chunks, ragged last chunk
+    (2, 777, 48, 16, "f32", 100, False),      # chunk rounded up to 112 steps
+    (1, 300, 16, 32, "f32", 48, True),
+    (1, 257, 40, 64, "bf16", 128, True),      # ragged channel tile too
+]
+
+
+@pytest.mark.parametrize("b,L,D,N,dt,q,with_h0", CHUNK_CASES)
+def test_chunked_sequence_matches_oracle_and_single_chunk(cuda_dev, b, L, D, N, dt, q, with_h0):
+    """The sequence split into chunks (local pass, carry, output pass) gives the oracle's
+    result and agrees with the one-chunk run up to fp32 rounding."""
+    inp = make_scan_inputs(b, L, D, N, dt, seed=4000 + L + D + N + q, d_skip="normal")
+    h0 = torch.randn(b, D, N, generator=torch.Generator().manual_seed(L)) if with_h0 else None
+    g = _to(cuda_dev, inp)
+    h0_d = h0.to(cuda_dev) if h0 is not None else None
+    y_c, h_c = ssm_scan_fwd(**g, h0=h0_d, chunk_len=q)
+    y_1, h_1 = ssm_scan_fwd(**g, h0=h0_d, chunk_len=L)
+    torch.cuda.synchronize()
+    y_ref, h_ref = oracle.ssm_scan_ref(**inp, h0=h0)
+    assert rel_l2(y_c.float().cpu().numpy(), y_ref) <= TOL_Y[dt]
+    assert rel_l2(h_c.cpu().numpy(), h_ref) <= TOL_H[dt]
+    assert rel_l2(h_c.cpu().numpy(), h_1.cpu().numpy()) <= 2e-6
+    assert rel_l2(y_c.float().cpu().numpy(), y_1.float().cpu().numpy()) <= (2e-6 if dt == "f32" else 4e-3)
+    assert device_status() == binding.SSM_OK
+
+
+def test_automatic_split_for_few_channels(cuda_dev):
+    """One channel tile and a long sequence: the library splits the sequence by itself and
+    asks for workspace; the result matches the oracle."""
+    inp = make_scan_inputs(1, 4096, 16, 16, "bf16", seed=4242)
+    g = _to(cuda_dev, inp)
+    lib = binding.load_library()
+    y, h = ssm_scan_fwd(**g)
+    torch.cuda.synchronize()
+    y_ref, h_ref = oracle.ssm_scan_ref(**inp)
+    assert rel_l2(y.float().cpu().numpy(), y_ref) <= TOL_Y["bf16"]
+    assert rel_l2(h.cpu().numpy(), h_ref) <= TOL_H["bf16"]
+    assert binding.scan_workspace_size(**g) > 0

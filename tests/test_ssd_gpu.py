@@ -1,4 +1,13 @@
-"""GPU parity of the SSD chunked scan (through the C ABI) against the fp64 oracle."""
+"""GPU parity of the SSD chunked scan (through the C ABI) against the fp64 oracle.
+
+Shapes with bf16 I/O, P = 64, N = 128 and a chunk that is a multiple of 128 take the
+tensor-core kernel; the others take the CUDA-core recurrence kernel.
+
+Tolerances: rel-L2 <= 1e-5 for fp32 I/O and <= 2e-2 for bf16 I/O on y. The final state is
+fp32; on the tensor-core path the MMA operands w*x (the decayed inputs of the state update)
+and the carried state (operand of C S) are rounded to bf16, a relative error of at most 2^-9
+per element that averages to about 1e-3 over the 128-term products, so h_last is held to
+5e-3 for bf16 inputs."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +20,7 @@ from conftest import rel_l2
 pytestmark = pytest.mark.gpu
 
 TOL_Y = {"f32": 1e-5, "bf16": 2e-2}
-TOL_H = {"f32": 1e-5, "bf16": 1e-4}
+TOL_H = {"f32": 1e-5, "bf16": 5e-3}
 
 
 def _to(dev, inp):
@@ -73,3 +82,39 @@ def test_full_size_workload_on_sampled_heads(cuda_dev):
     print(f"SSD workload: rel-L2 y {ey:.3e}  h_last {eh:.3e}")
     assert ey <= TOL_Y["bf16"]
     assert eh <= TOL_H["bf16"]
+
+
+TC_CASES = [
+    # b, L, H, P, N, G, Q, gate, dskip, h0
+    (1, 128, 2, 64, 128, 1, 128, False, False, False),
+    (2, 333, 4, 64, 128, 2, 128, True, True, True),     # ragged last block, 2 groups, D, z, h0
+    (1, 77, 3, 64, 128, 1, 256, False, True, False),    # shorter than one block
+    (2, 1000, 2, 64, 128, 1, 256, False, False, True),
+]
+
+
+@pytest.mark.parametrize("b,L,H,P,N,G,Q,gate,dskip,with_h0", TC_CASES)
+def test_tensor_core_path_matches_oracle_and_cuda_core_path(cuda_dev, b, L, H, P, N, G, Q, gate, dskip, with_h0):
+    inp = make_ssd_inputs(b, L, H, P, N, "bf16", seed=900 + L + H + G, d_skip="normal" if dskip else "none",
+                          gate=gate, ngroups=G)
+    h0 = torch.randn(b, H, N, P, generator=torch.Generator().manual_seed(L)) if with_h0 else None
+    g = _to(cuda_dev, inp)
+    h0_d = h0.to(cuda_dev) if h0 is not None else None
+    y_tc, h_tc = ssd_chunk_scan_fwd(**g, chunk_size=Q, h0=h0_d)
+    y_cc, h_cc = ssd_chunk_scan_fwd(**g, chunk_size=64, h0=h0_d)     # not a multiple of 128: CUDA cores
+    torch.cuda.synchronize()
+    y_ref, h_ref = oracle.ssd_scan_ref(**inp, h0=h0)
+    assert rel_l2(y_tc.float().cpu().numpy(), y_ref) <= TOL_Y["bf16"]
+    assert rel_l2(h_tc.cpu().numpy(), h_ref) <= TOL_H["bf16"]
+    assert rel_l2(y_cc.float().cpu().numpy(), y_ref) <= TOL_Y["bf16"]
+    assert rel_l2(h_cc.cpu().numpy(), h_ref) <= 1e-4
+    assert rel_l2(y_tc.float().cpu().numpy(), y_cc.float().cpu().numpy()) <= TOL_Y["bf16"]
+
+
+def test_tensor_core_path_empty_sequence_copies_h0(cuda_dev):
+    inp = make_ssd_inputs(1, 0, 2, 64, 128, "bf16", seed=5)
+    g = _to(cuda_dev, inp)
+    h0 = torch.randn(1, 2, 128, 64, device=cuda_dev)
+    y, h = ssd_chunk_scan_fwd(**g, chunk_size=256, h0=h0)
+    torch.cuda.synchronize()
+    assert y.shape == (1, 0, 2, 64) and torch.equal(h, h0)
