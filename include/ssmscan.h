@@ -125,6 +125,29 @@ SSMSCAN_API size_t ssm_scan_workspace_size(const ssm_scan_params* p);
 SSMSCAN_API ssm_status_t ssm_scan_fwd(const ssm_scan_params* p, void* stream);
 
 /*
+ * Allocation-free variant of ssm_scan_fwd. The pages have no counterpart: it serves callers
+ * that cannot allocate device memory or pass a workspace (for example a host application
+ * whose device memory is fixed at start-up, or a plugin inside another runtime that owns all
+ * device allocations), and callers that cannot afford cudaMalloc's implicit synchronisation.
+ *  - Same arguments and results as ssm_scan_fwd; p->workspace and p->workspace_bytes are
+ *    ignored. Inputs and outputs are still the caller's.
+ *  - The scratch of the chunked (long-sequence) path comes from a buffer compiled into the
+ *    library, SSM_NOALLOC_SCRATCH_BYTES (16 MiB) of device memory on every GPU that loads the
+ *    library, held until the process exits. A call that needs more
+ *    (ssm_scan_workspace_size(p) > SSM_NOALLOC_SCRATCH_BYTES) returns SSM_ERR_UNSUPPORTED
+ *    before anything is launched; a larger chunk_len needs less.
+ *  - The first call on a device looks up the buffer's device address (cudaGetSymbolAddress)
+ *    with that device current; make that first call before any stream capture.
+ *  - Every call shares the one buffer, which keeps the last call's contents (nothing in it has
+ *    to start at zero: each call writes every element it later reads). Calls whose work
+ *    overlaps on the GPU (different streams, or different host threads) race on it: serialise
+ *    them.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define SSM_NOALLOC_SCRATCH_BYTES (16u << 20)
+SSMSCAN_API ssm_status_t ssm_scan_fwd_noalloc(const ssm_scan_params* p, void* stream);
+
+/*
  * Mamba-2 SSD chunked scan: the same recurrence with one scalar A per head and the state
  * an N x P matrix per (batch, head):
  *   dt_t = softplus(delta[b,t,h] + delta_bias[h]);  S = exp(dt_t A_h) S + dt_t B_t (x) x_t

@@ -25,7 +25,8 @@ ABI_VERSION = 1
 # Every function the header declares (checked by the CPU test suite).
 EXPORTS = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssd_chunk_scan_workspace_size", "ssd_chunk_scan_fwd",
            "ssm_device_status", "ssm_status_string", "ssm_last_error", "ssm_abi_version",
-           "ssm_kernel_launch_count")
+           "ssm_kernel_launch_count", "ssm_scan_fwd_noalloc")
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _i64, _i32, _vp, _sz = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
 
@@ -86,6 +87,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.ssm_last_error.restype = ctypes.c_char_p
             lib.ssm_abi_version.argtypes = []
             lib.ssm_abi_version.restype = ctypes.c_int
+            lib.ssm_scan_fwd_noalloc.argtypes = [ctypes.POINTER(ScanParams), _vp]
+            lib.ssm_scan_fwd_noalloc.restype = ctypes.c_int
             lib.ssm_kernel_launch_count.argtypes = []
             lib.ssm_kernel_launch_count.restype = ctypes.c_uint64
             if lib.ssm_abi_version() != ABI_VERSION:
@@ -216,6 +219,19 @@ def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_so
         p.workspace, p.workspace_bytes = _ptr(ws), ws.numel()
     with torch.cuda.device(x.device):
         _check(lib, lib.ssm_scan_fwd(ctypes.byref(p), _stream_handle(stream)))
+    return y, hl
+
+
+def ssm_scan_fwd_noalloc(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_softplus=True, h0=None,
+                         chunk_len=0, out=None, return_last_state=True, h_last=None, stream=None):
+    """The allocation-free C entry point (no workspace: the library's built-in scratch is
+    used). Outputs are allocated here when not given; pass ``out`` and ``h_last`` to keep the
+    call itself free of allocations. Returns (y, h_last or None)."""
+    lib = load_library()
+    p, y, hl = _scan_params(x, delta, A, B, C, D, z, delta_bias, delta_softplus=delta_softplus, h0=h0,
+                            chunk_len=chunk_len, out=out, return_last_state=return_last_state, h_last=h_last)
+    with torch.cuda.device(x.device):
+        _check(lib, lib.ssm_scan_fwd_noalloc(ctypes.byref(p), _stream_handle(stream)))
     return y, hl
 
 

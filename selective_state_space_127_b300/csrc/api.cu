@@ -205,6 +205,12 @@ ssm_status_t validate_ssd(const ssd_scan_params* p, ssm::SSDArgs* out) {
 
 }  // namespace
 
+namespace ssm {
+// Record a reason for ssm_last_error() on the calling thread and return `s` (for entry points
+// defined in other files of the library).
+ssm_status_t set_error(ssm_status_t s, const char* msg) { return fail(s, "%s", msg); }
+}  // namespace ssm
+
 extern "C" {
 
 size_t ssm_scan_workspace_size(const ssm_scan_params* p) {

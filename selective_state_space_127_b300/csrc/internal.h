@@ -54,6 +54,9 @@ struct SSDArgs {
 // Which selective-scan kernel a call takes.
 enum class ScanPath { Generic = 0, Fast = 1, ChunkCarry = 2 };
 
+// Record a reason for ssm_last_error() on the calling thread; returns `s`.
+ssm_status_t set_error(ssm_status_t s, const char* msg);
+
 // Count of kernels enqueued by this library (reported through ssm_kernel_launch_count).
 void note_launches(int n);
 
