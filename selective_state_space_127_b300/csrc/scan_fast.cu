@@ -4,22 +4,22 @@
 //
 // Work split. A CTA owns kCh = 16 consecutive channels of one batch row and walks one
 // chunk of the sequence (the whole sequence when it is not split). LPC lanes share a
-// channel, each keeping N / LPC fp32 states in registers.
+// channel, lane g keeping the fp32 states n in [g S, g S + S), S = N / LPC, in registers.
 //
-// Per tile of kT = 16 steps:
-//  1. TMA (3-D maps over (D or N, L, b)) has brought x, delta, z, B and C into a kStages
-//     ring guarded by mbarriers.
-//  2. Producer phase, all threads: for each (step, channel) the scalars that do not depend
-//     on the state, dt = softplus(delta + bias), u = dt x, silu(z) and D x, computed once
-//     (two channels per thread) and written to shared memory as (dt, dt, u, u) and
-//     (D x, silu z); B and C are widened to fp32. The ring slot is then refilled.
-//  3. Update phase: lane g of channel c, per step, reads (dt, dt, u, u) and its B, C
-//     slices with 16-byte loads and runs, on packed fp32 pairs (f32x2),
-//        A_bar = 2^(dt * A log2 e)            SFU ex2, one per state
-//        h     = A_bar h + u B                fma.rn.f32x2 / mul.rn.f32x2
-//        y    += C h
-//     then the LPC lanes' partial sums of LPC consecutive steps are reduce-scattered with
-//     shuffles so lane g finishes step g as (y + D x) silu(z); y leaves by TMA store.
+// Data movement. TMA (3-D tensor maps over (D or N, L, b)) streams 32-step tiles of x,
+// delta, z, B and C into a 3-deep shared-memory ring guarded by mbarriers; y tiles leave
+// through TMA stores from a double buffer. B and C tiles are widened to fp32 once per tile
+// by the CTA, so lanes then read their states' values with 8- or 16-byte loads.
+//
+// Steps go in groups of LPC. Lane g of a channel computes the per-(t, channel) scalars of
+// step g of the group (dt = softplus(delta + bias), dt x, silu(z), D x) one group ahead, so
+// that chain overlaps the state updates of the current group; the (dt, dt x) pairs are then
+// broadcast inside the channel's lanes. Per step and state:
+//   A_bar[n] = 2^(dt * A[n] * log2 e)           SFU ex2
+//   h[n] = A_bar[n] h[n] + (dt x) B[n]          packed fp32 pairs (fma.rn.f32x2)
+//   y += C[n] h[n]                               packed pairs
+// and the lanes' partial sums of the LPC steps are reduce-scattered (log2 LPC shuffle
+// rounds), leaving lane g with step g's y, which it finishes as (y + D x) silu(z).
 //
 // Chunked sequence (long sequences with few channels, where one CTA per channel tile
 // would leave most SMs idle):
@@ -38,7 +38,6 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
-#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -49,8 +48,8 @@ namespace ssm {
 namespace {
 
 constexpr int kCh = 16;        // channels per CTA
-constexpr int kT = 16;         // steps per tile
-constexpr int kStages = 4;     // TMA ring depth
+constexpr int kT = 32;         // steps per tile
+constexpr int kStages = 3;     // TMA ring depth
 
 enum Mode { kFull = 0, kPass1 = 1 };
 
@@ -79,37 +78,53 @@ struct Layout {
     static constexpr int kStageStride = (kStageBytes + 127) / 128 * 128;
     static constexpr int kBars = 0;                                   // kStages mbarriers
     static constexpr int kRing = 128;
-    static constexpr int kSc = kRing + kStages * kStageStride;        // float4 (dt, dt, u, u) [kT][kCh]
-    static constexpr int kEg = kSc + kT * kCh * 16;                   // float2 (D x, silu z) [kT][kCh]
-    static constexpr int kBCf = kEg + kT * kCh * 8;                   // fp32 B then C [kT][N]
+    static constexpr int kBCf = kRing + kStages * kStageStride;       // fp32 B then C [kT][N]
     static constexpr int kY = kBCf + 2 * kT * N * 4;                  // 2 y tiles
     static constexpr int kYStride = (kTileX + 127) / 128 * 128;
     static constexpr int kTotal = kY + 2 * kYStride;
 };
 
-// Two consecutive I/O elements (bf16 or fp32) of a shared-memory tile as floats.
-template <bool BF16>
-__device__ __forceinline__ void ld_pair(const unsigned char* tile, int idx, float& a, float& b) {
-    if constexpr (BF16) {
-        const uint32_t v = *reinterpret_cast<const uint32_t*>(tile + idx * 2);
-        a = __uint_as_float(v << 16);
-        b = __uint_as_float(v & 0xffff0000u);
+__device__ __forceinline__ float ld_io(const void* base, int i, bool bf16) {
+    return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]) : static_cast<const float*>(base)[i];
+}
+
+// Per-(step, channel) scalars one lane computes for its step of a group.
+struct Scal {
+    float dt, u, dx, gate;
+};
+
+template <bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS>
+__device__ __forceinline__ Scal scalars(const void* xs, const void* ds, const void* zs, int jj, int c, float bias,
+                                        float Dd, bool tv) {
+    Scal r;
+    const float xr = ld_io(xs, jj * kCh + c, BF16);
+    float dt = ld_io(ds, jj * kCh + c, BF16) + bias;
+    if constexpr (SOFTPLUS) dt = softplus_fast(dt);
+    r.dt = tv ? dt : 0.f;
+    r.u = r.dt * xr;
+    r.dx = DSKIP ? Dd * xr : 0.f;
+    r.gate = GATE ? silu_fast(ld_io(zs, jj * kCh + c, BF16)) : 1.f;
+    return r;
+}
+
+// S consecutive fp32 values of a shared-memory row as S / 2 packed pairs.
+template <int S>
+__device__ __forceinline__ void lds_pairs(const float* p, f2 (&v)[S / 2]) {
+    if constexpr (S % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < S / 2; k += 2) {
+            const ulonglong2 q = *reinterpret_cast<const ulonglong2*>(p + 2 * k);
+            v[k] = q.x;
+            v[k + 1] = q.y;
+        }
     } else {
-        const float2 v = *reinterpret_cast<const float2*>(tile + idx * 4);
-        a = v.x;
-        b = v.y;
+#pragma unroll
+        for (int k = 0; k < S / 2; ++k) v[k] = *reinterpret_cast<const unsigned long long*>(p + 2 * k);
     }
 }
 
-// Sixteen bytes of shared memory as two packed fp32 pairs.
-__device__ __forceinline__ void lds_2xf2(const float* p, f2& lo, f2& hi) {
-    const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(p);
-    lo = v.x;
-    hi = v.y;
-}
-
 template <int N, bool BF16, int LPC, bool GATE, bool DSKIP, bool SOFTPLUS, int MODE>
-__global__ void __launch_bounds__(kCh * LPC)
+__global__ void __launch_bounds__(kCh * LPC, 16 / LPC)
 scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap md,
                  const __grid_constant__ CUtensorMap mz, const __grid_constant__ CUtensorMap mB,
                  const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap my,
@@ -120,13 +135,10 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
     constexpr int P = S / 2;           // packed pairs per lane
     constexpr bool kReadout = MODE == kFull;
     constexpr bool kGate = GATE && kReadout;
-    static_assert(S % 4 == 0, "states per lane must be a multiple of 4");
-    static_assert(LPC == 2 || LPC == 4, "2 or 4 lanes per channel");
+    static_assert(S % 2 == 0, "states per lane must be even");
+    static_assert(LPC == 2 || LPC == 4 || LPC == 8, "2, 4 or 8 lanes per channel");
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBars);
-    float4* sc = reinterpret_cast<float4*>(smem + Lay::kSc);
-    float2* eg = reinterpret_cast<float2*>(smem + Lay::kEg);
-    float* bcf = reinterpret_cast<float*>(smem + Lay::kBCf);
 
     const int tid = threadIdx.x;
     const int c = tid / LPC, g = tid % LPC;
@@ -165,25 +177,9 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         A2[k] = pk(a0, a1);
         h[k] = pk(h0v, h1v);
     }
-
-    // producer role: thread handles channel pair cp (fixed) and rows r0, r0 + kRowStep, ...
-    constexpr int kPairs = kCh / 2;
-    constexpr int kRowStep = kThreads / kPairs;
-    const int cp = tid % kPairs;
-    const int r0 = tid / kPairs;
-    float pb0 = 0.f, pb1 = 0.f, pD0 = 0.f, pD1 = 0.f;
-    {
-        const int e0 = d0 + 2 * cp, e1 = e0 + 1;
-        if (p.bias) {
-            pb0 = e0 < p.dim ? p.bias[e0] : 0.f;
-            pb1 = e1 < p.dim ? p.bias[e1] : 0.f;
-        }
-        if (DSKIP) {
-            pD0 = e0 < p.dim ? p.D[e0] : 0.f;
-            pD1 = e1 < p.dim ? p.D[e1] : 0.f;
-        }
-    }
-    float dtsum = 0.f;   // pass 1: sum of dt over the chunk (lane 0 of each channel)
+    const float bias = (dvalid && p.bias) ? p.bias[d] : 0.f;
+    const float Dd = (DSKIP && dvalid) ? p.D[d] : 0.f;
+    float dtsum = 0.f;   // pass 1: sum of dt over the chunk
 
     auto stage_ptr = [&](int buf) { return smem + Lay::kRing + buf * Lay::kStageStride; };
     auto issue = [&](int s) {
@@ -211,8 +207,6 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
     bool failed = false;
     for (int s = 0; s < ntiles; ++s) {
         const int buf = s % kStages;
-        const int rem = (int)(len - (int64_t)s * kT);
-        const int tcount = rem < kT ? rem : kT;
         const bool ok = mbar_wait_bounded(&bars[buf], (s / kStages) & 1, p.status);
         if (__syncthreads_or(!ok)) {
             // give up on this tile; before leaving, wait (bounded) for the later tiles
@@ -223,40 +217,13 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
             failed = true;
             break;
         }
-        const unsigned char* st = stage_ptr(buf);
-
-        // ---------------- producer phase
-#pragma unroll
-        for (int r = r0; r < kT; r += kRowStep) {
-            const int idx = r * kCh + 2 * cp;
-            float x0, x1, v0, v1;
-            ld_pair<BF16>(st, idx, x0, x1);
-            ld_pair<BF16>(st + Lay::kTileX, idx, v0, v1);
-            v0 += pb0;
-            v1 += pb1;
-            if constexpr (SOFTPLUS) {
-                v0 = softplus_fast(v0);
-                v1 = softplus_fast(v1);
-            }
-            const bool tv = r < tcount;
-            const float dt0 = tv ? v0 : 0.f, dt1 = tv ? v1 : 0.f;
-            const float u0 = dt0 * x0, u1 = dt1 * x1;
-            sc[r * kCh + 2 * cp] = make_float4(dt0, dt0, u0, u0);
-            sc[r * kCh + 2 * cp + 1] = make_float4(dt1, dt1, u1, u1);
-            if constexpr (kReadout) {
-                float g0 = 1.f, g1 = 1.f;
-                if constexpr (kGate) {
-                    float z0, z1;
-                    ld_pair<BF16>(st + 2 * Lay::kTileX, idx, z0, z1);
-                    g0 = silu_fast(z0);
-                    g1 = silu_fast(z1);
-                }
-                *reinterpret_cast<float4*>(&eg[r * kCh + 2 * cp]) =
-                    make_float4(DSKIP ? pD0 * x0 : 0.f, g0, DSKIP ? pD1 * x1 : 0.f, g1);
-            }
-        }
+        unsigned char* st = stage_ptr(buf);
+        const void* xs = st;
+        const void* ds = st + Lay::kTileX;
+        const void* zs = st + 2 * Lay::kTileX;
+        // B (and C) of the tile widened to fp32
+        float* bcf = reinterpret_cast<float*>(smem + Lay::kBCf);
         if constexpr (BF16) {
-            // B then C: kReadout ? 2 : 1 tiles of kT * N bf16, widened to fp32
             const uint4* src = reinterpret_cast<const uint4*>(st + 3 * Lay::kTileX);
             constexpr int kChunks = (kReadout ? 2 : 1) * kT * N / 8;
 #pragma unroll
@@ -274,63 +241,42 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
 #pragma unroll
             for (int i = tid; i < kChunks; i += kThreads) reinterpret_cast<float4*>(bcf)[i] = src[i];
         }
+        const float* Bf = bcf;
+        const float* Cf = bcf + kT * N;
         unsigned char* ys = smem + Lay::kY + (s & 1) * Lay::kYStride;
         if (kReadout && s >= 2 && tid == 0) tma_store_wait_read<1>();   // the store of tile s-2 read ys
         __syncthreads();
-        // the ring slot has been consumed: refill it
-        if (tid == 0 && s + kStages < ntiles) issue(s + kStages);
+        const int rem = (int)(len - (int64_t)s * kT);
+        const int tcount = rem < kT ? rem : kT;
 
-        // ---------------- update phase
-        const float* Bf = bcf;
-        const float* Cf = bcf + kT * N;
         float yout[kT / LPC];   // the steps this lane finishes; stored after the loop so that no
                                 // shared-memory store sits between the loads of later steps
-        // The state-independent work of a group of LPC steps (A_bar, u B, C) is done one group
-        // ahead of the dependent state updates, so SFU and shared-memory latency overlap them.
-        f2 ab[2][LPC][P], vv[2][LPC][P], cc[2][LPC][P];
-        auto prepare = [&](int grp, int slot) {
-#pragma unroll
-            for (int q = 0; q < LPC; ++q) {
-                const int t = grp * LPC + q;
-                f2 dt2, u2;
-                lds_2xf2(reinterpret_cast<const float*>(&sc[t * kCh + c]), dt2, u2);
-                if constexpr (MODE == kPass1) {
-                    if (g == 0) {
-                        float lo, hi;
-                        upk(dt2, lo, hi);
-                        dtsum += lo;
-                    }
-                }
-                const float* Brow = Bf + t * N + g * S;
-                const float* Crow = Cf + t * N + g * S;
-#pragma unroll
-                for (int k = 0; k < P; k += 2) {
-                    f2 b01, b23;
-                    lds_2xf2(Brow + 2 * k, b01, b23);
-                    float e0, e1, e2, e3;
-                    upk(mul2(dt2, A2[k]), e0, e1);
-                    upk(mul2(dt2, A2[k + 1]), e2, e3);
-                    ab[slot][q][k] = pk(ex2_approx(e0), ex2_approx(e1));
-                    ab[slot][q][k + 1] = pk(ex2_approx(e2), ex2_approx(e3));
-                    vv[slot][q][k] = mul2(u2, b01);
-                    vv[slot][q][k + 1] = mul2(u2, b23);
-                    if constexpr (kReadout) lds_2xf2(Crow + 2 * k, cc[slot][q][k], cc[slot][q][k + 1]);
-                }
-            }
-        };
-        prepare(0, 0);
+        Scal cur = scalars<BF16, kGate, DSKIP && kReadout, SOFTPLUS>(xs, ds, zs, g, c, bias, Dd, g < tcount);
 #pragma unroll
         for (int grp = 0; grp < kT / LPC; ++grp) {
-            const int cur = grp & 1;
-            if (grp + 1 < kT / LPC) prepare(grp + 1, cur ^ 1);
+            // the next group's scalars: independent of the state, overlaps the updates below
+            const int jn = (grp + 1) * LPC + g;
+            const Scal nxt = scalars<BF16, kGate, DSKIP && kReadout, SOFTPLUS>(xs, ds, zs, jn < kT ? jn : g, c, bias,
+                                                                              Dd, jn < tcount);
             float acc[LPC];
 #pragma unroll
             for (int q = 0; q < LPC; ++q) {
+                const float dtq = __shfl_sync(0xffffffffu, cur.dt, q, LPC);
+                const float uq = __shfl_sync(0xffffffffu, cur.u, q, LPC);
+                if constexpr (MODE == kPass1) dtsum += dtq;
+                const f2 dt2 = pk(dtq, dtq), u2 = pk(uq, uq);
+                f2 bv[P];
+                lds_pairs<S>(Bf + (grp * LPC + q) * N + g * S, bv);
+                f2 cv[P];
+                if constexpr (kReadout) lds_pairs<S>(Cf + (grp * LPC + q) * N + g * S, cv);
                 f2 a2 = pk(0.f, 0.f);
 #pragma unroll
                 for (int k = 0; k < P; ++k) {
-                    h[k] = fma2(ab[cur][q][k], h[k], vv[cur][q][k]);
-                    if constexpr (kReadout) a2 = fma2(cc[cur][q][k], h[k], a2);
+                    float e0, e1;
+                    upk(mul2(dt2, A2[k]), e0, e1);
+                    const f2 ab = pk(ex2_approx(e0), ex2_approx(e1));
+                    h[k] = fma2(ab, h[k], mul2(u2, bv[k]));
+                    if constexpr (kReadout) a2 = fma2(cv[k], h[k], a2);
                 }
                 if constexpr (kReadout) {
                     float lo, hi;
@@ -339,22 +285,22 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
                 }
             }
             if constexpr (kReadout) {
-                // reduce-scatter over the LPC lanes of the channel: lane g ends with step g's sum
-                float tot;
-                if constexpr (LPC == 4) {
-                    const bool hi2 = (g & 2) != 0;
-                    const float ra = (hi2 ? acc[2] : acc[0]) + __shfl_xor_sync(0xffffffffu, hi2 ? acc[0] : acc[2], 2);
-                    const float rb = (hi2 ? acc[3] : acc[1]) + __shfl_xor_sync(0xffffffffu, hi2 ? acc[1] : acc[3], 2);
-                    const bool hi1 = (g & 1) != 0;
-                    tot = (hi1 ? rb : ra) + __shfl_xor_sync(0xffffffffu, hi1 ? ra : rb, 1);
-                } else {
-                    const bool hi1 = (g & 1) != 0;
-                    tot = (hi1 ? acc[1] : acc[0]) + __shfl_xor_sync(0xffffffffu, hi1 ? acc[0] : acc[1], 1);
+                // reduce-scatter over the LPC lanes of the channel: each round a lane keeps the
+                // half of its partial sums whose step index has its lane bit and adds the
+                // partner's; lane g ends with the full sum of step g
+#pragma unroll
+                for (int m = LPC / 2; m >= 1; m >>= 1) {
+                    const bool upper = (g & m) != 0;
+#pragma unroll
+                    for (int i = 0; i < m; ++i) {
+                        const float keep = upper ? acc[i + m] : acc[i];
+                        const float send = upper ? acc[i] : acc[i + m];
+                        acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                    }
                 }
-                const int jj = grp * LPC + g;
-                const float2 e = eg[jj * kCh + c];
-                yout[grp] = (tot + e.x) * e.y;
+                yout[grp] = (acc[0] + cur.dx) * cur.gate;
             }
+            cur = nxt;
         }
         if constexpr (kReadout) {
 #pragma unroll
@@ -365,12 +311,15 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
                 else
                     reinterpret_cast<float*>(ys)[jj * kCh + c] = yout[grp];
             }
+            fence_proxy_async_smem();
         }
-        if constexpr (kReadout) fence_proxy_async_smem();
         __syncthreads();
-        if (kReadout && tid == 0) {
-            tma_store_3d(&my, d0, (int)(t_begin + (int64_t)s * kT), b, ys);
-            tma_store_commit();
+        if (tid == 0) {
+            if constexpr (kReadout) {
+                tma_store_3d(&my, d0, (int)(t_begin + (int64_t)s * kT), b, ys);
+                tma_store_commit();
+            }
+            if (s + kStages < ntiles) issue(s + kStages);
         }
     }
     if (kReadout && tid == 0) tma_store_wait_all();
@@ -453,20 +402,16 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t inner, int64_
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// Lanes per channel: 2 for N = 16 (8 states a lane), 4 above.
+// Lanes per channel: N / 8, so every lane keeps 8 states (4 packed pairs). Measured on the
+// b8 D1536 L2048 N16 bf16 workload: 2 lanes 177 us, 4 lanes 194 us, 8 lanes 236 us -- eight
+// independent state chains per lane hide the SFU and shared-memory latency better than more
+// warps with fewer states each.
 template <int N>
-constexpr int lanes_per_channel() { return N == 16 ? 2 : 4; }
+constexpr int lanes_per_channel() { return N / 8; }
 
 template <int N, bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS, int MODE, int LPC = lanes_per_channel<N>()>
 cudaError_t launch_t(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz, cudaStream_t st) {
     using Lay = Layout<N, BF16>;
-    if constexpr (N == 16 && LPC == 2) {
-        static const bool four = [] {
-            const char* e = getenv("SSMSCAN_N16_LANES");
-            return e && e[0] == '4';
-        }();
-        if (four) return launch_t<N, BF16, GATE, DSKIP, SOFTPLUS, MODE, 4>(maps, fp, a, nz, st);
-    }
     auto kern = scan_fast_kernel<N, BF16, LPC, GATE, DSKIP, SOFTPLUS, MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kTotal);
     if (e != cudaSuccess) return e;

@@ -8,10 +8,9 @@
 //
 //   G      = C B^T                                  (Q x Q, K = N)      tcgen05, TMEM
 //   M[t,s] = G[t,s] exp(cum_t - cum_s) dt_s, s <= t; 0 above the diagonal
-//   Y      = M X                                    (Q x P, K = Q)      tcgen05, A from TMEM
-//   Yoff   = C S_prev                               (Q x P, K = N)      tcgen05
-//   y_t    = Y_t + exp(cum_t) Yoff_t  (+ D x_t) (* silu z_t)
-//   S      = exp(cum_last) S_prev + B^T (w o X),    w_s = exp(cum_last - cum_s) dt_s
+//   Y      = M X + (exp(cum) o C) S_prev           (Q x P, K = Q + N)  tcgen05, M from TMEM
+//   y_t    = Y_t (+ D x_t) (* silu z_t)
+//   S      = exp(cum_last) S_prev + (w o B)^T X,    w_s = exp(cum_last - cum_s) dt_s
 //                                                   (N x P, K = Q)      tcgen05
 //
 // which is the block decomposition of the semiseparable matrix of the recurrence
@@ -22,10 +21,13 @@
 //
 // Data movement: TMA (4-D maps, 128-byte swizzle) brings the C and B blocks (128 x 128) and
 // the x block (128 x 64) into shared memory in the layouts the MMAs read directly (C and B
-// K-major for G and Yoff; B as the MN-major A operand of the state product; x MN-major as
-// the B operand); the y block leaves by TMA store from the x buffer. Tensor memory holds G
-// (128 columns, overwritten in place by the bf16 M as the A operand of M X, then by the state
-// product), Y (64) and Yoff (64): 256 columns, so two CTAs fit on an SM.
+// K-major for G; C, rescaled in place by exp(cum_t), K-major for the hand-off; B, rescaled
+// in place by w_s, as the MN-major A operand of the state product; x MN-major as the B
+// operand); the y block leaves by TMA store from the x buffer. The next block's C and B are
+// requested as soon as this block's products are done with them, its x once y has left.
+// Tensor memory: G (128 columns, overwritten in place by the bf16 M, then by the state
+// product) and Y (64): 256 columns allocated, so two CTAs share an SM. One thread issues the
+// MMAs and waits for them; the others wait at the CTA barrier.
 //
 // Pages: "Mamba-2 / Structured State Space Duality" (abeam) "基本アイデア" (SSM as a
 // semiseparable matrix; diagonal blocks by ordinary matrix products, off-diagonal blocks by a
@@ -48,11 +50,10 @@ constexpr int kP = 64;           // head dimension
 constexpr int kN = 128;          // state size
 constexpr int kThreads = 128;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColG = 0;    // G, then M (bf16 pairs, columns 0..63) and the state product (64..127)
+constexpr uint32_t kColG = 0;    // G (128 columns); then M in bf16 pairs (columns 0..63) and the state product (64..127)
 constexpr uint32_t kColM = 0;
 constexpr uint32_t kColS = 64;
-constexpr uint32_t kColY = 128;
-constexpr uint32_t kColYoff = 192;
+constexpr uint32_t kColY = 128;  // Y = M X + (exp(cum) o C) S_prev (64 columns)
 
 constexpr int kAtom = 16384;     // 128 rows x 128 bytes
 constexpr int kSmC = 0;
@@ -62,13 +63,12 @@ constexpr int kSmS = 5 * kAtom;
 constexpr int kSmCs = 6 * kAtom;             // float [kQ]: cum_t log2(e)
 constexpr int kSmDt = kSmCs + kQ * 4;        // float [kQ]: dt_t
 constexpr int kSmRed = kSmDt + kQ * 4;       // float [4]: warp totals of the scan
-constexpr int kSmBar = kSmRed + 64;          // 2 mbarriers
-constexpr int kSmTmem = kSmBar + 16;         // tensor-memory base address
+constexpr int kSmBar = kSmRed + 64;          // 4 mbarriers: C, B and x loads, MMA completion
+constexpr int kSmTmem = kSmBar + 32;         // tensor-memory base address
 constexpr int kSmemUsed = kSmTmem + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024; // room to align the base to 1024 bytes
 
 constexpr uint32_t kIdescG = tc::idesc_bf16(128, 128, false, false);
-constexpr uint32_t kIdescYoff = tc::idesc_bf16(128, 64, false, true);
 constexpr uint32_t kIdescY = tc::idesc_bf16(128, 64, false, true);
 constexpr uint32_t kIdescS = tc::idesc_bf16(128, 64, true, true);
 
@@ -126,8 +126,10 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
     float* cs = reinterpret_cast<float*>(sm + kSmCs);
     float* dts = reinterpret_cast<float*>(sm + kSmDt);
     float* red = reinterpret_cast<float*>(sm + kSmRed);
-    uint64_t* bar_load = reinterpret_cast<uint64_t*>(sm + kSmBar);
-    uint64_t* bar_mma = bar_load + 1;
+    uint64_t* bar_c = reinterpret_cast<uint64_t*>(sm + kSmBar);
+    uint64_t* bar_b = bar_c + 1;
+    uint64_t* bar_x = bar_c + 2;
+    uint64_t* bar_mma = bar_c + 3;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kSmTmem);
 
     const int tid = threadIdx.x;
@@ -139,7 +141,9 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
 
     if (warp == 0) tc::tmem_alloc(tslot, kTmemCols);
     if (tid == 0) {
-        mbar_init(bar_load, 1);
+        mbar_init(bar_c, 1);
+        mbar_init(bar_b, 1);
+        mbar_init(bar_x, 1);
         mbar_init(bar_mma, 1);
         fence_mbar_init();
         prefetch_tensormap(&mX);
@@ -183,26 +187,48 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
     const uint32_t aC = smem_u32(sC), aB = smem_u32(sB), aX = smem_u32(sX), aS = smem_u32(sS);
     const __nv_bfloat16* delta = static_cast<const __nv_bfloat16*>(p.delta);
 
-    unsigned ph_load = 0, ph_mma = 0;
+    // Load schedule: C and B of block j+1 once the products of block j are done with them,
+    // x of block j+1 once the y of block j (staged in the x buffer) has been read out by its
+    // TMA store.
+    auto load_c = [&](int j) {
+        mbar_arrive_expect_tx(bar_c, 2 * kAtom);
+        tma_load_4d(sC, &mC, 0, grp, j * kQ, b, bar_c);
+        tma_load_4d(sC + kAtom, &mC, 64, grp, j * kQ, b, bar_c);
+    };
+    auto load_b = [&](int j) {
+        mbar_arrive_expect_tx(bar_b, 2 * kAtom);
+        tma_load_4d(sB, &mB, 0, grp, j * kQ, b, bar_b);
+        tma_load_4d(sB + kAtom, &mB, 64, grp, j * kQ, b, bar_b);
+    };
+    auto load_x = [&](int j) {
+        mbar_arrive_expect_tx(bar_x, kAtom);
+        tma_load_4d(sX, &mX, 0, h, j * kQ, b, bar_x);
+    };
+    if (tid == 0 && p.nblocks > 0) {
+        load_c(0);
+        load_b(0);
+        load_x(0);
+    }
+    // delta of row t, one block ahead
+    auto load_delta = [&](int j) -> float {
+        const int64_t tt = (int64_t)j * kQ + tid;
+        return (j < p.nblocks && tt < L) ? __bfloat162float(delta[((int64_t)b * L + tt) * H + h]) : 0.f;
+    };
+    float draw_next = load_delta(0);
+
+    unsigned ph_mma = 0;
     bool failed = false;
     for (int j = 0; j < p.nblocks; ++j) {
         const int t0 = j * kQ;
-        if (tid == 0) {
-            if (j > 0) tma_store_wait_read<0>();   // the previous y block has left sX
-            mbar_arrive_expect_tx(bar_load, 4 * kAtom + kAtom);
-            tma_load_4d(sC, &mC, 0, grp, t0, b, bar_load);
-            tma_load_4d(sC + kAtom, &mC, 64, grp, t0, b, bar_load);
-            tma_load_4d(sB, &mB, 0, grp, t0, b, bar_load);
-            tma_load_4d(sB + kAtom, &mB, 64, grp, t0, b, bar_load);
-            tma_load_4d(sX, &mX, 0, h, t0, b, bar_load);
-        }
+        const unsigned ph_ld = j & 1;
         // dt_t and the inclusive cumulative sum of dt A_h over the block (row t = tid)
         const int64_t t = t0 + tid;
         float dt = 0.f;
         if (t < L) {
-            float v = __bfloat162float(delta[((int64_t)b * L + t) * H + h]) + bias;
+            const float v = draw_next + bias;
             dt = p.softplus ? softplus_accurate(v) : v;
         }
+        draw_next = load_delta(j + 1);
         float cum = dt * Ah;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -224,33 +250,53 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
         const float e_t = ex2_approx(cs_t);
         const float e_last = ex2_approx(cum_last * kLog2e);
 
-        const bool ok = mbar_wait_bounded(bar_load, ph_load, p.status);
-        ph_load ^= 1;
+        // G = C B^T (one thread issues and waits; the others wait at the barrier)
+        bool ok = true;
+        if (tid == 0) {
+            ok = mbar_wait_bounded(bar_c, ph_ld, p.status) && mbar_wait_bounded(bar_b, ph_ld, p.status);
+            if (ok) {
+                tc::fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < kN / 16; ++k) {
+                    const uint32_t off = (k / 4) * kAtom + (k % 4) * 32;
+                    tc::mma_ss(tmem + kColG, tc::sdesc_sw128(aC + off, 16, 1024),
+                               tc::sdesc_sw128(aB + off, 16, 1024), kIdescG, k > 0);
+                }
+                tc::commit(bar_mma);
+                ok = mbar_wait_bounded(bar_mma, ph_mma, p.status);
+            }
+        }
+        ph_mma ^= 1;
         if (__syncthreads_or(!ok)) {
             failed = true;
             break;
         }
-        // G = C B^T and Yoff = C S_prev
-        if (tid == 0) {
-            tc::fence_after_sync();
-#pragma unroll
-            for (int k = 0; k < kN / 16; ++k) {
-                const uint32_t off = (k / 4) * kAtom + (k % 4) * 32;
-                tc::mma_ss(tmem + kColG, tc::sdesc_sw128(aC + off, 16, 1024), tc::sdesc_sw128(aB + off, 16, 1024),
-                           kIdescG, k > 0);
-            }
-#pragma unroll
-            for (int k = 0; k < kN / 16; ++k) {
-                const uint32_t off = (k / 4) * kAtom + (k % 4) * 32;
-                tc::mma_ss(tmem + kColYoff, tc::sdesc_sw128(aC + off, 16, 1024),
-                           tc::sdesc_sw128(aS + k * 2048, kAtom, 1024), kIdescYoff, k > 0);
-            }
-            tc::commit(bar_mma);
-        }
-        if (!mbar_wait_bounded(bar_mma, ph_mma, p.status)) failed = true;
-        ph_mma ^= 1;
         tc::fence_after_sync();
 
+        // G has read C and B: scale them in place, row t of C by exp(cum_t) (the decay from the
+        // block start, so that (exp(cum) o C) S_prev is the state hand-off) and row s of B by
+        // w_s = exp(cum_last - cum_s) dt_s (the weights of the state product (w o B)^T X)
+#pragma unroll
+        for (int atom = 0; atom < 2; ++atom) {
+            uint4* rowc = reinterpret_cast<uint4*>(sC + atom * kAtom + tid * 128);
+            uint4* rowb = reinterpret_cast<uint4*>(sB + atom * kAtom + tid * 128);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int c = i ^ (tid & 7);   // rows t..t+7 start on different 16-byte bank groups
+                uint4 v = rowc[c];
+                v.x = tc::pack_bf16(bf_lo(v.x) * e_t, bf_hi(v.x) * e_t);
+                v.y = tc::pack_bf16(bf_lo(v.y) * e_t, bf_hi(v.y) * e_t);
+                v.z = tc::pack_bf16(bf_lo(v.z) * e_t, bf_hi(v.z) * e_t);
+                v.w = tc::pack_bf16(bf_lo(v.w) * e_t, bf_hi(v.w) * e_t);
+                rowc[c] = v;
+                uint4 u = rowb[c];
+                u.x = tc::pack_bf16(bf_lo(u.x) * w_t, bf_hi(u.x) * w_t);
+                u.y = tc::pack_bf16(bf_lo(u.y) * w_t, bf_hi(u.y) * w_t);
+                u.z = tc::pack_bf16(bf_lo(u.z) * w_t, bf_hi(u.z) * w_t);
+                u.w = tc::pack_bf16(bf_lo(u.w) * w_t, bf_hi(u.w) * w_t);
+                rowb[c] = u;
+            }
+        }
         // M[t, s] = G[t, s] exp(cum_t - cum_s) dt_s for s <= t, written in place over G as
         // bf16 pairs (columns 16 kc .. 16 kc + 15 after columns 32 kc .. 32 kc + 31 are read)
 #pragma unroll 1
@@ -261,12 +307,16 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
                 tc::ld32(lane_base + kColG + 32 * kc, r);
                 tc::wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
+                for (int i = 0; i < 32; i += 4) {
                     const int s0 = 32 * kc + i;
-                    const float m0 = s0 <= tid ? __uint_as_float(r[i]) * ex2_approx(cs_t - cs[s0]) * dts[s0] : 0.f;
-                    const float m1 =
-                        s0 + 1 <= tid ? __uint_as_float(r[i + 1]) * ex2_approx(cs_t - cs[s0 + 1]) * dts[s0 + 1] : 0.f;
+                    const float4 c4 = *reinterpret_cast<const float4*>(cs + s0);
+                    const float4 d4 = *reinterpret_cast<const float4*>(dts + s0);
+                    const float m0 = s0 <= tid ? __uint_as_float(r[i]) * ex2_approx(cs_t - c4.x) * d4.x : 0.f;
+                    const float m1 = s0 + 1 <= tid ? __uint_as_float(r[i + 1]) * ex2_approx(cs_t - c4.y) * d4.y : 0.f;
+                    const float m2 = s0 + 2 <= tid ? __uint_as_float(r[i + 2]) * ex2_approx(cs_t - c4.z) * d4.z : 0.f;
+                    const float m3 = s0 + 3 <= tid ? __uint_as_float(r[i + 3]) * ex2_approx(cs_t - c4.w) * d4.w : 0.f;
                     packed[i / 2] = tc::pack_bf16(m0, m1);
+                    packed[i / 2 + 1] = tc::pack_bf16(m2, m3);
                 }
             } else {
 #pragma unroll
@@ -275,52 +325,43 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
             tc::st16(lane_base + kColM + 16 * kc, packed);
         }
         tc::wait_st();
+        fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncthreads();
-        // Y = M X
+        // Y = M X + (exp(cum) o C) S_prev and S_acc = (w o B)^T X
         if (tid == 0) {
-            tc::fence_after_sync();
+            ok = mbar_wait_bounded(bar_x, ph_ld, p.status);
+            if (ok) {
+                tc::fence_after_sync();
 #pragma unroll
-            for (int k = 0; k < kQ / 16; ++k)
-                tc::mma_ts(tmem + kColY, tmem + kColM + 8 * k, tc::sdesc_sw128(aX + k * 2048, kAtom, 1024), kIdescY,
-                           k > 0);
-            tc::commit(bar_mma);
-        }
-        if (!mbar_wait_bounded(bar_mma, ph_mma, p.status)) failed = true;
-        ph_mma ^= 1;
-        tc::fence_after_sync();
-
-        // x row s (= tid) scaled in place by w_s: the B operand of the state product
-        {
-            uint4* row = reinterpret_cast<uint4*>(sX + tid * 128);
+                for (int k = 0; k < kQ / 16; ++k)
+                    tc::mma_ts(tmem + kColY, tmem + kColM + 8 * k, tc::sdesc_sw128(aX + k * 2048, kAtom, 1024),
+                               kIdescY, k > 0);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 v = row[c];
-                v.x = tc::pack_bf16(bf_lo(v.x) * w_t, bf_hi(v.x) * w_t);
-                v.y = tc::pack_bf16(bf_lo(v.y) * w_t, bf_hi(v.y) * w_t);
-                v.z = tc::pack_bf16(bf_lo(v.z) * w_t, bf_hi(v.z) * w_t);
-                v.w = tc::pack_bf16(bf_lo(v.w) * w_t, bf_hi(v.w) * w_t);
-                row[c] = v;
+                for (int k = 0; k < kN / 16; ++k) {
+                    const uint32_t off = (k / 4) * kAtom + (k % 4) * 32;
+                    tc::mma_ss(tmem + kColY, tc::sdesc_sw128(aC + off, 16, 1024),
+                               tc::sdesc_sw128(aS + k * 2048, kAtom, 1024), kIdescY, 1);
+                }
+#pragma unroll
+                for (int k = 0; k < kQ / 16; ++k)
+                    tc::mma_ss(tmem + kColS, tc::sdesc_sw128(aB + k * 2048, kAtom, 1024),
+                               tc::sdesc_sw128(aX + k * 2048, kAtom, 1024), kIdescS, k > 0);
+                tc::commit(bar_mma);
+                ok = mbar_wait_bounded(bar_mma, ph_mma, p.status);
+            }
+            // C and B of this block are no longer read
+            if (ok && j + 1 < p.nblocks) {
+                load_c(j + 1);
+                load_b(j + 1);
             }
         }
-        fence_proxy_async_smem();
-        __syncthreads();
-        // S_acc = B^T (w o X)
-        if (tid == 0) {
-            tc::fence_after_sync();
-#pragma unroll
-            for (int k = 0; k < kQ / 16; ++k)
-                tc::mma_ss(tmem + kColS, tc::sdesc_sw128(aB + k * 2048, kAtom, 1024),
-                           tc::sdesc_sw128(aX + k * 2048, kAtom, 1024), kIdescS, k > 0);
-            tc::commit(bar_mma);
-        }
-        if (!mbar_wait_bounded(bar_mma, ph_mma, p.status)) failed = true;
         ph_mma ^= 1;
-        tc::fence_after_sync();
-        if (__syncthreads_or(failed)) {
+        if (__syncthreads_or(!ok)) {
             failed = true;
             break;
         }
+        tc::fence_after_sync();
 
         // epilogue: y row t = tid into sX (free now), the state row n = tid
         const __nv_bfloat16* xrow =
@@ -329,13 +370,12 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
             p.z && t < L ? static_cast<const __nv_bfloat16*>(p.z) + (((int64_t)b * L + t) * H + h) * kP : nullptr;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            uint32_t ry[32], ro[32];
+            uint32_t ry[32];
             tc::ld32(lane_base + kColY + 32 * half, ry);
-            tc::ld32(lane_base + kColYoff + 32 * half, ro);
             tc::wait_ld();
             float yv[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) yv[i] = fmaf(e_t, __uint_as_float(ro[i]), __uint_as_float(ry[i]));
+            for (int i = 0; i < 32; ++i) yv[i] = __uint_as_float(ry[i]);
             if (xrow) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 8) {
@@ -397,6 +437,10 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
         if (tid == 0) {
             tma_store_4d(&mY, 0, h, t0, b, sX);
             tma_store_commit();
+            if (j + 1 < p.nblocks) {
+                tma_store_wait_read<0>();   // y has left the x buffer
+                load_x(j + 1);
+            }
         }
     }
     if (tid == 0) tma_store_wait_all();
