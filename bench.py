@@ -92,6 +92,33 @@ def ssd_flops(w):
     return cb + diag + off + state
 
 
+def ssd_mma_flops(w, block=128):
+    """Flops the tensor-core SSD kernel executes: per (batch, head, 128-step block) the dense
+    products G = C B^T (2*Q*Q*N), Y = M X (2*Q*Q*P), the hand-off (exp(cum) o C) S_prev
+    (2*Q*N*P) and the state product (w o B)^T X (2*Q*N*P)."""
+    nblk = (w.seqlen + block - 1) // block
+    per = 2 * block * block * w.dstate + 2 * block * block * w.headdim + 4 * block * w.dstate * w.headdim
+    return w.batch * w.nheads * nblk * per
+
+
+def profiled_traffic(kernel_file, summary):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) recorded in a
+    profile summary under profiles/, if that summary was taken of the current source of the
+    kernel (its sha256 matches); else None."""
+    import hashlib
+    import re
+    src = os.path.join(ROOT, "selective_state_space_127_b300", "csrc", kernel_file)
+    path = os.path.join(ROOT, "profiles", summary)
+    if not (os.path.exists(src) and os.path.exists(path)):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha256:\s*([0-9a-f]{64})", text)
+    if not m:
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return int(m.group(1)) if digest == m.group(2) else None
+
+
 # ------------------------------------------------------------------ clocks during the timed region
 
 class ClockSampler:
@@ -298,7 +325,8 @@ def run_ours(args):
         "hbm_frac": round(gbs_rank / peaks["hbm_gbs"], 4),
         "hbm_peak_gbs": peaks["hbm_gbs"], "peak_source": peak_src,
         "roofline": {"bound": "alu", "achieved": round(achieved_upd, 1), "peak": round(alu_peak, 1),
-                     "unit": "Gupdate/s", "frac": round(achieved_upd / alu_peak, 4), "traffic": None,
+                     "unit": "Gupdate/s", "frac": round(achieved_upd / alu_peak, 4),
+                     "traffic": profiled_traffic("scan_fast.cu", "scan_fast_b8_D1536_L2048_N16_bf16.md"),
                      "kernel": "selective scan", "algorithmic_bytes": nbytes, "updates": updates,
                      "peak_basis": f"{UPDATES_PER_CLK_SM:.0f} updates/clk/SM x {SMS} SMs x {mhz_peak:.0f} MHz "
                                    "(ex2 and FP32-lane limits, measured)"},
@@ -319,10 +347,19 @@ def run_ours(args):
         sms = _max_over_ranks(_timed(sstep, ssteps, max(3, min(args.warmup, 5)), stream, barrier), dev, world)
         fl = ssd_flops(sw)
         tf = fl / (sms * 1e-3) / 1e12
+        mma = ssd_mma_flops(sw)
+        mma_tf = mma / (sms * 1e-3) / 1e12
         result["ssd"] = {"workload": sw.name, "ms_per_step": round(sms, 4), "steps": ssteps,
                          "value": round(tf * world, 3), "unit": "TFLOP/s", "flops_per_step": fl,
+                         "flops_basis": "algorithmic: causal halves, C B^T once per (batch, 256-step chunk)",
                          "gbs": round(ssd_bytes(sw) / (sms * 1e-3) / 1e9 * world, 1),
-                         "tensor_frac_of_bf16_burst": round(tf / peaks["bf16_tflops"], 4)}
+                         "hbm_frac": round(ssd_bytes(sw) / (sms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                         "roofline": {"bound": "tensor", "achieved": round(mma_tf, 1),
+                                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                                      "frac": round(mma_tf / peaks["bf16_tflops"], 4),
+                                      "traffic": profiled_traffic("ssd_tc.cu", "ssd_tc_b4_H64_P64_N128_L4096_bf16.md"),
+                                      "kernel": "ssd_tc_kernel", "mma_flops_per_launch": mma,
+                                      "peak_basis": "measured bf16 dense burst (cuBLAS 8192^3)"}}
         del sinp, sy, shl
 
     if args.extra_workloads:
