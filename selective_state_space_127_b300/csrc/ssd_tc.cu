@@ -1,8 +1,8 @@
 // Mamba-2 SSD chunked scan on the fifth-generation tensor cores (tcgen05), for bf16 I/O with
 // head dimension P = 64 and state size N = 128.
 //
-// One CTA (128 threads) per (batch, head) walks the sequence in blocks of Q = 128 steps;
-// the N x P state S stays on chip (fp32 registers, thread n holding row n, plus a bf16 copy
+// One CTA (256 threads) per (batch, head) walks the sequence in blocks of Q = 128 steps;
+// the N x P state S stays on chip (fp32 registers, two threads per row n, plus a bf16 copy
 // in shared memory as an MMA operand). Per block, with cum_t the inclusive cumulative sum of
 // dt A_h inside the block (the decay from the block start to step t):
 //
@@ -25,9 +25,10 @@
 // in place by w_s, as the MN-major A operand of the state product; x MN-major as the B
 // operand); the y block leaves by TMA store from the x buffer. The next block's C and B are
 // requested as soon as this block's products are done with them, its x once y has left.
-// Tensor memory: G (128 columns, overwritten in place by the bf16 M, then by the state
-// product) and Y (64): 256 columns allocated, so two CTAs share an SM. One thread issues the
-// MMAs and waits for them; the others wait at the CTA barrier.
+// Tensor memory: G (128 columns, then the state product), M in bf16 (64) and Y (64): 256
+// columns, so two CTAs share an SM. Eight warps: two per TMEM lane quarter (the rows a warp
+// may access), splitting the columns of the mask, scaling and epilogue work between them.
+// One thread issues the MMAs and waits for them; the others wait at the CTA barrier.
 //
 // Pages: "Mamba-2 / Structured State Space Duality" (abeam) "基本アイデア" (SSM as a
 // semiseparable matrix; diagonal blocks by ordinary matrix products, off-diagonal blocks by a
@@ -48,12 +49,12 @@ namespace {
 constexpr int kQ = 128;          // steps per block
 constexpr int kP = 64;           // head dimension
 constexpr int kN = 128;          // state size
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;    // 8 warps: two per TMEM lane quarter, splitting the columns
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColG = 0;    // G (128 columns); then M in bf16 pairs (columns 0..63) and the state product (64..127)
-constexpr uint32_t kColM = 0;
-constexpr uint32_t kColS = 64;
-constexpr uint32_t kColY = 128;  // Y = M X + (exp(cum) o C) S_prev (64 columns)
+constexpr uint32_t kColG = 0;    // G (128 columns); after the mask pass the state product (0..63)
+constexpr uint32_t kColS = 0;
+constexpr uint32_t kColM = 128;  // M in bf16 pairs (64 columns)
+constexpr uint32_t kColY = 192;  // Y = M X + (exp(cum) o C) S_prev (64 columns)
 
 constexpr int kAtom = 16384;     // 128 rows x 128 bytes
 constexpr int kSmC = 0;
@@ -61,8 +62,10 @@ constexpr int kSmB = 2 * kAtom;
 constexpr int kSmX = 4 * kAtom;
 constexpr int kSmS = 5 * kAtom;
 constexpr int kSmCs = 6 * kAtom;             // float [kQ]: cum_t log2(e)
-constexpr int kSmDt = kSmCs + kQ * 4;        // float [kQ]: dt_t
-constexpr int kSmRed = kSmDt + kQ * 4;       // float [4]: warp totals of the scan
+constexpr int kSmLw = kSmCs + kQ * 4;        // float [kQ]: dt_s
+constexpr int kSmEv = kSmLw + kQ * 4;        // float [kQ]: exp(cum_t)
+constexpr int kSmWv = kSmEv + kQ * 4;        // float [kQ]: exp(cum_last - cum_s) dt_s
+constexpr int kSmRed = kSmWv + kQ * 4;       // float [8]: warp totals of the scan, exp(cum_last)
 constexpr int kSmBar = kSmRed + 64;          // 4 mbarriers: C, B and x loads, MMA completion
 constexpr int kSmTmem = kSmBar + 32;         // tensor-memory base address
 constexpr int kSmemUsed = kSmTmem + 16;
@@ -113,7 +116,22 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, int c0, int
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
-__global__ void __launch_bounds__(kThreads)
+// Eight bf16 values (16 bytes) times a scalar held as a packed pair, rounded back to bf16.
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 v, f2 s2) {
+    float a, c;
+    uint4 r;
+    upk(mul2(pk(bf_lo(v.x), bf_hi(v.x)), s2), a, c);
+    r.x = tc::pack_bf16(a, c);
+    upk(mul2(pk(bf_lo(v.y), bf_hi(v.y)), s2), a, c);
+    r.y = tc::pack_bf16(a, c);
+    upk(mul2(pk(bf_lo(v.z), bf_hi(v.z)), s2), a, c);
+    r.z = tc::pack_bf16(a, c);
+    upk(mul2(pk(bf_lo(v.w), bf_hi(v.w)), s2), a, c);
+    r.w = tc::pack_bf16(a, c);
+    return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
 ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUtensorMap mB,
               const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap mY, const TcParams p) {
     extern __shared__ unsigned char smem_raw[];
@@ -123,8 +141,10 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
     unsigned char* sB = sm + kSmB;
     unsigned char* sX = sm + kSmX;
     unsigned char* sS = sm + kSmS;
-    float* cs = reinterpret_cast<float*>(sm + kSmCs);
-    float* dts = reinterpret_cast<float*>(sm + kSmDt);
+    float* cs = reinterpret_cast<float*>(sm + kSmCs);    // cum_t log2 e
+    float* lw = reinterpret_cast<float*>(sm + kSmLw);    // dt_s
+    float* ev = reinterpret_cast<float*>(sm + kSmEv);    // exp(cum_t)
+    float* wv = reinterpret_cast<float*>(sm + kSmWv);    // exp(cum_last - cum_s) dt_s
     float* red = reinterpret_cast<float*>(sm + kSmRed);
     uint64_t* bar_c = reinterpret_cast<uint64_t*>(sm + kSmBar);
     uint64_t* bar_b = bar_c + 1;
@@ -134,6 +154,9 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3;        // the TMEM lanes (rows) this warp can access
+    const int half = warp >> 2;          // which half of the columns (or atom) it takes
+    const int row = tid & 127;           // = 32 quarter + lane
     const int h = blockIdx.x, b = blockIdx.y;
     const int grp = h / p.heads_per_group;
     const int64_t L = p.seqlen;
@@ -152,12 +175,13 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
         prefetch_tensormap(&mY);
     }
 
-    // the state: thread n holds row n (P fp32 values); its bf16 copy is the B operand of C S
-    float S[kP];
+    // the state: row `row`, columns [32 half, 32 half + 32) in fp32 registers; its bf16 copy
+    // (the B operand of the hand-off product) in sS
+    float S[kP / 2];
     {
-        const float* src = p.h0 ? p.h0 + (((int64_t)b * H + h) * kN + tid) * kP : nullptr;
+        const float* src = p.h0 ? p.h0 + (((int64_t)b * H + h) * kN + row) * kP + 32 * half : nullptr;
 #pragma unroll
-        for (int i = 0; i < kP; i += 4) {
+        for (int i = 0; i < kP / 2; i += 4) {
             const float4 v = src ? *reinterpret_cast<const float4*>(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
             S[i] = v.x;
             S[i + 1] = v.y;
@@ -165,13 +189,13 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
             S[i + 3] = v.w;
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 4; ++j) {
             uint4 v;
             v.x = tc::pack_bf16(S[8 * j], S[8 * j + 1]);
             v.y = tc::pack_bf16(S[8 * j + 2], S[8 * j + 3]);
             v.z = tc::pack_bf16(S[8 * j + 4], S[8 * j + 5]);
             v.w = tc::pack_bf16(S[8 * j + 6], S[8 * j + 7]);
-            *reinterpret_cast<uint4*>(sS + sw128(tid, j)) = v;
+            *reinterpret_cast<uint4*>(sS + sw128(row, 4 * half + j)) = v;
         }
     }
     fence_proxy_async_smem();
@@ -179,7 +203,7 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * warp) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
 
     const float Ah = p.A[h];
     const float bias = p.bias ? p.bias[h] : 0.f;
@@ -209,10 +233,10 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
         load_b(0);
         load_x(0);
     }
-    // delta of row t, one block ahead
+    // delta of row t (threads of the first warpgroup), one block ahead
     auto load_delta = [&](int j) -> float {
-        const int64_t tt = (int64_t)j * kQ + tid;
-        return (j < p.nblocks && tt < L) ? __bfloat162float(delta[((int64_t)b * L + tt) * H + h]) : 0.f;
+        const int64_t tt = (int64_t)j * kQ + row;
+        return (half == 0 && j < p.nblocks && tt < L) ? __bfloat162float(delta[((int64_t)b * L + tt) * H + h]) : 0.f;
     };
     float draw_next = load_delta(0);
 
@@ -221,34 +245,41 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
     for (int j = 0; j < p.nblocks; ++j) {
         const int t0 = j * kQ;
         const unsigned ph_ld = j & 1;
-        // dt_t and the inclusive cumulative sum of dt A_h over the block (row t = tid)
-        const int64_t t = t0 + tid;
-        float dt = 0.f;
-        if (t < L) {
-            const float v = draw_next + bias;
-            dt = p.softplus ? softplus_accurate(v) : v;
+        const int64_t t = t0 + row;
+        // dt_t and the inclusive cumulative sum of dt A_h over the block (first warpgroup, row t)
+        if (half == 0) {
+            float dt = 0.f;
+            if (t < L) {
+                const float v = draw_next + bias;
+                dt = p.softplus ? softplus_accurate(v) : v;
+            }
+            float cum = dt * Ah;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, cum, o);
+                if (lane >= o) cum += n;
+            }
+            if (lane == 31) red[warp] = cum;
+            cs[row] = cum;   // provisional: the warp-local prefix, completed below
+            lw[row] = dt;
         }
         draw_next = load_delta(j + 1);
-        float cum = dt * Ah;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float n = __shfl_up_sync(0xffffffffu, cum, o);
-            if (lane >= o) cum += n;
-        }
-        if (lane == 31) red[warp] = cum;
         __syncthreads();
-        float before = 0.f;
+        if (half == 0) {
+            float before = 0.f;
 #pragma unroll
-        for (int w = 0; w < 4; ++w)
-            if (w < warp) before += red[w];
-        cum += before;
-        const float cum_last = red[0] + red[1] + red[2] + red[3];
-        const float cs_t = cum * kLog2e;
-        cs[tid] = cs_t;
-        dts[tid] = dt;
-        const float w_t = ex2_approx((cum_last - cum) * kLog2e) * dt;
-        const float e_t = ex2_approx(cs_t);
-        const float e_last = ex2_approx(cum_last * kLog2e);
+            for (int w = 0; w < 4; ++w)
+                if (w < warp) before += red[w];
+            const float cum = cs[row] + before;
+            const float dt = lw[row];
+            const float cum_last = red[0] + red[1] + red[2] + red[3];
+            const float cs_t = cum * kLog2e;
+            cs[row] = cs_t;
+            lw[row] = dt;
+            ev[row] = ex2_approx(cs_t);
+            wv[row] = ex2_approx((cum_last - cum) * kLog2e) * dt;
+            if (row == 0) red[4] = ex2_approx(cum_last * kLog2e);
+        }
 
         // G = C B^T (one thread issues and waits; the others wait at the barrier)
         bool ok = true;
@@ -272,53 +303,61 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
             break;
         }
         tc::fence_after_sync();
+        const float cs_t = cs[row];
+        const float e_last = red[4];
 
         // G has read C and B: scale them in place, row t of C by exp(cum_t) (the decay from the
         // block start, so that (exp(cum) o C) S_prev is the state hand-off) and row s of B by
-        // w_s = exp(cum_last - cum_s) dt_s (the weights of the state product (w o B)^T X)
-#pragma unroll
-        for (int atom = 0; atom < 2; ++atom) {
-            uint4* rowc = reinterpret_cast<uint4*>(sC + atom * kAtom + tid * 128);
-            uint4* rowb = reinterpret_cast<uint4*>(sB + atom * kAtom + tid * 128);
+        // w_s = exp(cum_last - cum_s) dt_s (the weights of the state product (w o B)^T X).
+        // Thread (row, half) takes atom `half` of the row; the chunks are walked in swizzled
+        // order so that eight consecutive rows hit eight different bank groups.
+        {
+            const f2 e2 = pk(ev[row], ev[row]);
+            const f2 w2 = pk(wv[row], wv[row]);
+            uint4* rowc = reinterpret_cast<uint4*>(sC + half * kAtom + row * 128);
+            uint4* rowb = reinterpret_cast<uint4*>(sB + half * kAtom + row * 128);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const int c = i ^ (tid & 7);   // rows t..t+7 start on different 16-byte bank groups
-                uint4 v = rowc[c];
-                v.x = tc::pack_bf16(bf_lo(v.x) * e_t, bf_hi(v.x) * e_t);
-                v.y = tc::pack_bf16(bf_lo(v.y) * e_t, bf_hi(v.y) * e_t);
-                v.z = tc::pack_bf16(bf_lo(v.z) * e_t, bf_hi(v.z) * e_t);
-                v.w = tc::pack_bf16(bf_lo(v.w) * e_t, bf_hi(v.w) * e_t);
-                rowc[c] = v;
-                uint4 u = rowb[c];
-                u.x = tc::pack_bf16(bf_lo(u.x) * w_t, bf_hi(u.x) * w_t);
-                u.y = tc::pack_bf16(bf_lo(u.y) * w_t, bf_hi(u.y) * w_t);
-                u.z = tc::pack_bf16(bf_lo(u.z) * w_t, bf_hi(u.z) * w_t);
-                u.w = tc::pack_bf16(bf_lo(u.w) * w_t, bf_hi(u.w) * w_t);
-                rowb[c] = u;
+                const int c = i ^ (row & 7);
+                rowc[c] = scale_bf16x8(rowc[c], e2);
+                rowb[c] = scale_bf16x8(rowb[c], w2);
             }
         }
-        // M[t, s] = G[t, s] exp(cum_t - cum_s) dt_s for s <= t, written in place over G as
-        // bf16 pairs (columns 16 kc .. 16 kc + 15 after columns 32 kc .. 32 kc + 31 are read)
-#pragma unroll 1
-        for (int kc = 0; kc < 4; ++kc) {
+        // M[t, s] = G[t, s] exp(cum_t - cum_s) dt_s for s <= t (bf16 pairs in columns kColM..):
+        // warp (quarter, half) takes the 32-column chunks kc = half and half + 2 of its rows
+#pragma unroll
+        for (int ic = 0; ic < 2; ++ic) {
+            const int kc = half + 2 * ic;
             uint32_t packed[16];
-            if (kc <= warp) {            // warp-uniform: column blocks above the diagonal stay zero
+            if (kc < quarter) {          // below the diagonal: every s < t
                 uint32_t r[32];
                 tc::ld32(lane_base + kColG + 32 * kc, r);
                 tc::wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
-                    const int s0 = 32 * kc + i;
-                    const float4 c4 = *reinterpret_cast<const float4*>(cs + s0);
-                    const float4 d4 = *reinterpret_cast<const float4*>(dts + s0);
-                    const float m0 = s0 <= tid ? __uint_as_float(r[i]) * ex2_approx(cs_t - c4.x) * d4.x : 0.f;
-                    const float m1 = s0 + 1 <= tid ? __uint_as_float(r[i + 1]) * ex2_approx(cs_t - c4.y) * d4.y : 0.f;
-                    const float m2 = s0 + 2 <= tid ? __uint_as_float(r[i + 2]) * ex2_approx(cs_t - c4.z) * d4.z : 0.f;
-                    const float m3 = s0 + 3 <= tid ? __uint_as_float(r[i + 3]) * ex2_approx(cs_t - c4.w) * d4.w : 0.f;
+                    const float4 c4 = *reinterpret_cast<const float4*>(cs + 32 * kc + i);
+                    const float4 d4 = *reinterpret_cast<const float4*>(lw + 32 * kc + i);
+                    packed[i / 2] = tc::pack_bf16(__uint_as_float(r[i]) * d4.x * ex2_approx(cs_t - c4.x),
+                                                  __uint_as_float(r[i + 1]) * d4.y * ex2_approx(cs_t - c4.y));
+                    packed[i / 2 + 1] = tc::pack_bf16(__uint_as_float(r[i + 2]) * d4.z * ex2_approx(cs_t - c4.z),
+                                                      __uint_as_float(r[i + 3]) * d4.w * ex2_approx(cs_t - c4.w));
+                }
+            } else if (kc == quarter) {  // the diagonal chunk: s <= t
+                uint32_t r[32];
+                tc::ld32(lane_base + kColG + 32 * kc, r);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 c4 = *reinterpret_cast<const float4*>(cs + 32 * kc + i);
+                    const float4 d4 = *reinterpret_cast<const float4*>(lw + 32 * kc + i);
+                    const float m0 = i <= lane ? __uint_as_float(r[i]) * d4.x * ex2_approx(cs_t - c4.x) : 0.f;
+                    const float m1 = i + 1 <= lane ? __uint_as_float(r[i + 1]) * d4.y * ex2_approx(cs_t - c4.y) : 0.f;
+                    const float m2 = i + 2 <= lane ? __uint_as_float(r[i + 2]) * d4.z * ex2_approx(cs_t - c4.z) : 0.f;
+                    const float m3 = i + 3 <= lane ? __uint_as_float(r[i + 3]) * d4.w * ex2_approx(cs_t - c4.w) : 0.f;
                     packed[i / 2] = tc::pack_bf16(m0, m1);
                     packed[i / 2 + 1] = tc::pack_bf16(m2, m3);
                 }
-            } else {
+            } else {                     // above the diagonal
 #pragma unroll
                 for (int i = 0; i < 16; ++i) packed[i] = 0u;
             }
@@ -328,7 +367,7 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
         fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncthreads();
-        // Y = M X + (exp(cum) o C) S_prev and S_acc = (w o B)^T X
+        // Y = M X + (exp(cum) o C) S_prev and S_acc = (w o B)^T X (S_acc over G's columns)
         if (tid == 0) {
             ok = mbar_wait_bounded(bar_x, ph_ld, p.status);
             if (ok) {
@@ -363,23 +402,26 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
         }
         tc::fence_after_sync();
 
-        // epilogue: y row t = tid into sX (free now), the state row n = tid
-        const __nv_bfloat16* xrow =
-            p.D && t < L ? static_cast<const __nv_bfloat16*>(p.x) + (((int64_t)b * L + t) * H + h) * kP : nullptr;
-        const __nv_bfloat16* zrow =
-            p.z && t < L ? static_cast<const __nv_bfloat16*>(p.z) + (((int64_t)b * L + t) * H + h) * kP : nullptr;
+        // epilogue: y row t, columns [32 half, +32) into sX (free now); the state row, same
+        // columns; 16 columns at a time
+        const __nv_bfloat16* xrow = p.D && t < L ? static_cast<const __nv_bfloat16*>(p.x) +
+                                                       (((int64_t)b * L + t) * H + h) * kP + 32 * half
+                                                 : nullptr;
+        const __nv_bfloat16* zrow = p.z && t < L ? static_cast<const __nv_bfloat16*>(p.z) +
+                                                       (((int64_t)b * L + t) * H + h) * kP + 32 * half
+                                                 : nullptr;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint32_t ry[32];
-            tc::ld32(lane_base + kColY + 32 * half, ry);
+        for (int q = 0; q < 2; ++q) {
+            uint32_t ry[16];
+            tc::ld16(lane_base + kColY + 32 * half + 16 * q, ry);
             tc::wait_ld();
-            float yv[32];
+            float yv[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) yv[i] = __uint_as_float(ry[i]);
+            for (int i = 0; i < 16; ++i) yv[i] = __uint_as_float(ry[i]);
             if (xrow) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(xrow + 32 * half + i);
+                for (int i = 0; i < 16; i += 8) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(xrow + 16 * q + i);
                     yv[i] = fmaf(Dh, bf_lo(v.x), yv[i]);
                     yv[i + 1] = fmaf(Dh, bf_hi(v.x), yv[i + 1]);
                     yv[i + 2] = fmaf(Dh, bf_lo(v.y), yv[i + 2]);
@@ -392,8 +434,8 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
             }
             if (zrow) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 8) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(zrow + 32 * half + i);
+                for (int i = 0; i < 16; i += 8) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(zrow + 16 * q + i);
                     yv[i] *= silu_accurate(bf_lo(v.x));
                     yv[i + 1] *= silu_accurate(bf_hi(v.x));
                     yv[i + 2] *= silu_accurate(bf_lo(v.y));
@@ -405,31 +447,31 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
                 }
             }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint4 v;
                 v.x = tc::pack_bf16(yv[8 * c], yv[8 * c + 1]);
                 v.y = tc::pack_bf16(yv[8 * c + 2], yv[8 * c + 3]);
                 v.z = tc::pack_bf16(yv[8 * c + 4], yv[8 * c + 5]);
                 v.w = tc::pack_bf16(yv[8 * c + 6], yv[8 * c + 7]);
-                *reinterpret_cast<uint4*>(sX + sw128(tid, 4 * half + c)) = v;
+                *reinterpret_cast<uint4*>(sX + sw128(row, 4 * half + 2 * q + c)) = v;
             }
         }
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint32_t rs[32];
-            tc::ld32(lane_base + kColS + 32 * half, rs);
+        for (int q = 0; q < 2; ++q) {
+            uint32_t rs[16];
+            tc::ld16(lane_base + kColS + 32 * half + 16 * q, rs);
             tc::wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) S[32 * half + i] = fmaf(e_last, S[32 * half + i], __uint_as_float(rs[i]));
-        }
+            for (int i = 0; i < 16; ++i) S[16 * q + i] = fmaf(e_last, S[16 * q + i], __uint_as_float(rs[i]));
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint4 v;
-            v.x = tc::pack_bf16(S[8 * c], S[8 * c + 1]);
-            v.y = tc::pack_bf16(S[8 * c + 2], S[8 * c + 3]);
-            v.z = tc::pack_bf16(S[8 * c + 4], S[8 * c + 5]);
-            v.w = tc::pack_bf16(S[8 * c + 6], S[8 * c + 7]);
-            *reinterpret_cast<uint4*>(sS + sw128(tid, c)) = v;
+            for (int c = 0; c < 2; ++c) {
+                uint4 v;
+                v.x = tc::pack_bf16(S[16 * q + 8 * c], S[16 * q + 8 * c + 1]);
+                v.y = tc::pack_bf16(S[16 * q + 8 * c + 2], S[16 * q + 8 * c + 3]);
+                v.z = tc::pack_bf16(S[16 * q + 8 * c + 4], S[16 * q + 8 * c + 5]);
+                v.w = tc::pack_bf16(S[16 * q + 8 * c + 6], S[16 * q + 8 * c + 7]);
+                *reinterpret_cast<uint4*>(sS + sw128(row, 4 * half + 2 * q + c)) = v;
+            }
         }
         fence_proxy_async_smem();
         tc::fence_before_sync();
@@ -445,9 +487,10 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
     }
     if (tid == 0) tma_store_wait_all();
     if (!failed && p.h_last) {
-        float* dst = p.h_last + (((int64_t)b * H + h) * kN + tid) * kP;
+        float* dst = p.h_last + (((int64_t)b * H + h) * kN + row) * kP + 32 * half;
 #pragma unroll
-        for (int i = 0; i < kP; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
+        for (int i = 0; i < kP / 2; i += 4)
+            *reinterpret_cast<float4*>(dst + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
     }
     tc::fence_before_sync();
     __syncthreads();
