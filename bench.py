@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--workload", type=int, default=1, choices=[1, 2, 3])
     ap.add_argument("--no-ssd", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra-workloads", action="store_true", help="also time scan workloads 2 and 3")
     return ap.parse_args()
@@ -361,6 +362,24 @@ def run_ours(args):
                                       "kernel": "ssd_tc_kernel", "mma_flops_per_launch": mma,
                                       "peak_basis": "measured bf16 dense burst (cuBLAS 8192^3)"}}
         del sinp, sy, shl
+
+    if not args.no_decode:
+        # single-token recurrent step with the state advanced in place, workload 1's shapes
+        dinp = {k: (v[:, :1].contiguous() if k in ("x", "delta", "B", "C", "z") else v) for k, v in inp.items()}
+        dstate = torch.zeros(w.batch, w.dim, w.dstate, device=dev, dtype=torch.float32)
+        dy = torch.empty_like(dinp["x"])
+
+        def dstep():
+            ssm_scan_fwd(**dinp, h0=dstate, h_last=dstate, out=dy)
+
+        dsteps = 200
+        dms = _max_over_ranks(_timed(dstep, dsteps, 20, stream, barrier), dev, world)
+        state_bytes = 2 * w.batch * w.dim * w.dstate * 4
+        io_bytes = scan_bytes(w, seqlen=1) - w.batch * w.dim * w.dstate * 4
+        result["decode"] = {"workload": f"b{w.batch} D{w.dim} N{w.dstate} {w.dtype}, one token, state in place",
+                            "us_per_token": round(dms * 1e3, 3), "steps": dsteps,
+                            "gbs": round((state_bytes + io_bytes) / (dms * 1e-3) / 1e9 * world, 1),
+                            "bytes_per_token": state_bytes + io_bytes}
 
     if args.extra_workloads:
         extra = {}

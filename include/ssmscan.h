@@ -61,8 +61,8 @@ typedef enum { SSM_DISC_DELTA_B = 0, SSM_DISC_ZOH = 1 } ssm_discretization_t;
 /* Test hooks (debug_flags). SSM_DEBUG_SKIP_FIRST_LOAD: the TMA path never issues the copy
  * of its first tile, so its bounded wait runs out (about one second), the kernel latches
  * SSM_ERR_TIMEOUT in the device status word and returns with nothing in flight. Accepted
- * only when the whole sequence fits in that first tile (L <= 16) and the TMA path applies;
- * otherwise the call returns SSM_ERR_INVALID_ARG. */
+ * only when the whole sequence fits in that first tile (5 <= L <= 16) and the TMA path
+ * applies; otherwise the call returns SSM_ERR_INVALID_ARG. */
 #define SSM_DEBUG_SKIP_FIRST_LOAD 1
 
 /*
@@ -73,7 +73,10 @@ typedef enum { SSM_DISC_DELTA_B = 0, SSM_DISC_ZOH = 1 } ssm_discretization_t;
  *   y      = sum_n C[b,t,n] * h[n]  +  D[d] * x[b,t,d]
  *   y     *= silu(z[b,t,d]) = z / (1 + e^-z)
  * The output at t reads the state after x_t has entered it. The state starts at h0
- * (zeros when NULL) and its value after the last step is written to h_last.
+ * (zeros when NULL) and its value after the last step is written to h_last. h_last may be
+ * the same buffer as h0: with L = 1 that is the single-token (decode) step that advances a
+ * cached state in place ("Mamba/SSM complete guide" section 2: recurrent inference with a
+ * constant-size state).
  * Pages: "Mamba/SSM complete guide" section 5, listing `selective_scan` (discretise, loop,
  * readout, u*D) and MambaBlock.forward (y * silu(z)); "論文解説: Mamba" "選択機構"
  * (softplus) and "Hardware-Aware Parallel Scan" (the recurrence, zero initial state).

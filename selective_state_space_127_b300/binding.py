@@ -282,32 +282,76 @@ def ssd_chunk_scan_fwd(x, delta, A, B, C, chunk_size=256, D=None, z=None, delta_
     return y, hl
 
 
-def ssm_scan_fwd_host(inputs: dict, device="cuda", stream=None, dev_buffers: dict | None = None, **kw):
-    """End-to-end call for host buffers: copy the (pinned) host inputs to the device on the
-    stream, run ssm_scan_fwd, copy y and h_last back into pinned host tensors, synchronise.
-    ``dev_buffers`` may hold reusable device tensors keyed like ``inputs``."""
-    st = stream if stream is not None else torch.cuda.current_stream(device)
-    dev_in = {}
-    with torch.cuda.stream(st):
-        for k, v in inputs.items():
-            if v is None:
-                dev_in[k] = None
-                continue
-            buf = dev_buffers.get(k) if dev_buffers else None
-            if buf is None:
-                buf = torch.empty(v.shape, dtype=v.dtype, device=device)
-                if dev_buffers is not None:
-                    dev_buffers[k] = buf
-            buf.copy_(v, non_blocking=True)
-            dev_in[k] = buf
-        y, hl = ssm_scan_fwd(**dev_in, stream=st, **kw)
-        y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
-        y_host.copy_(y, non_blocking=True)
-        hl_host = None
-        if hl is not None:
-            hl_host = torch.empty(hl.shape, dtype=hl.dtype, pin_memory=True)
-            hl_host.copy_(hl, non_blocking=True)
-    st.synchronize()
+_PER_ROW = ("x", "delta", "z", "B", "C")
+
+
+def ssm_scan_fwd_host(inputs: dict, device="cuda", stream=None, dev_buffers: dict | None = None, slices=None,
+                      **kw):
+    """End-to-end call for pinned host buffers: copy the inputs to the device, run
+    ssm_scan_fwd, copy y and h_last back into pinned host tensors, synchronise.
+
+    Batch rows are independent, so the rows are split into ``slices`` groups (default
+    min(batch, 4)) whose host-to-device copy, scan and device-to-host copy run on three
+    streams (copy in, compute, copy out) and overlap across groups. ``dev_buffers`` (a
+    dict) keeps the device tensors, the pinned outputs and the streams between calls.
+    Returns (y_host, h_last_host)."""
+    dev = torch.device(device)
+    cache = dev_buffers if dev_buffers is not None else {}
+    x = inputs["x"]
+    b = x.shape[0]
+    nsl = max(1, min(b, slices or 4))
+    bounds = [(i * b // nsl, (i + 1) * b // nsl) for i in range(nsl)]
+    if "_streams" not in cache:
+        cache["_streams"] = tuple(torch.cuda.Stream(device=dev) for _ in range(3))
+    s_in, s_comp, s_out = cache["_streams"]
+    caller = stream if stream is not None else torch.cuda.current_stream(dev)
+    s_in.wait_stream(caller)
+
+    def dev_buf(name, like):
+        t = cache.get(name)
+        if t is None or t.shape != like.shape or t.dtype != like.dtype:
+            t = torch.empty(like.shape, dtype=like.dtype, device=dev)
+            cache[name] = t
+        return t
+
+    d = {k: (dev_buf(k, v) if v is not None else None) for k, v in inputs.items()}
+    N = inputs["A"].shape[1]
+    y_dev = dev_buf("_y", x)
+    hl_dev = dev_buf("_h_last", torch.empty((b, x.shape[2], N), dtype=torch.float32, device="meta"))
+    y_host = cache.get("_y_host")
+    if y_host is None or y_host.shape != x.shape or y_host.dtype != x.dtype:
+        y_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        cache["_y_host"] = y_host
+    hl_host = cache.get("_h_last_host")
+    if hl_host is None or hl_host.shape != hl_dev.shape:
+        hl_host = torch.empty(hl_dev.shape, dtype=torch.float32, pin_memory=True)
+        cache["_h_last_host"] = hl_host
+    with torch.cuda.stream(s_in):
+        for k, v in inputs.items():        # per-channel inputs: all at once
+            if v is not None and k not in _PER_ROW and k != "h0":
+                d[k].copy_(v, non_blocking=True)
+    for r0, r1 in bounds:
+        with torch.cuda.stream(s_in):
+            for k in _PER_ROW + ("h0",):
+                if inputs.get(k) is not None:
+                    d[k][r0:r1].copy_(inputs[k][r0:r1], non_blocking=True)
+        s_comp.wait_stream(s_in)
+        sl = {k: (v[r0:r1] if k in _PER_ROW else v) for k, v in d.items() if k != "h0"}
+        h0 = d["h0"][r0:r1] if d.get("h0") is not None else None
+        ckw = {k: v for k, v in kw.items() if k != "workspace"}
+        need = scan_workspace_size(**sl, h0=h0, **ckw)
+        ws = cache.get("_workspace")
+        if need > 0 and (ws is None or ws.numel() < need):
+            with torch.cuda.stream(s_comp):
+                ws = torch.empty(need, dtype=torch.uint8, device=dev)
+            cache["_workspace"] = ws
+        ssm_scan_fwd(**sl, h0=h0, out=y_dev[r0:r1], h_last=hl_dev[r0:r1], stream=s_comp,
+                     workspace=ws if need > 0 else None, **ckw)
+        s_out.wait_stream(s_comp)
+        with torch.cuda.stream(s_out):
+            y_host[r0:r1].copy_(y_dev[r0:r1], non_blocking=True)
+            hl_host[r0:r1].copy_(hl_dev[r0:r1], non_blocking=True)
+    s_out.synchronize()
     return y_host, hl_host
 
 

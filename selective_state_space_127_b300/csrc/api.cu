@@ -143,8 +143,12 @@ ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
     return SSM_OK;
 }
 
+// Sequences this short (a decode step is L = 1) take the generic kernel: one launch, no
+// TMA tile set-up, the state read once and written once (in place when h0 == h_last).
+constexpr int64_t kShortSeq = 4;
+
 size_t scan_workspace_bytes(const ssm::ScanArgs& a) {
-    return ssm::scan_fast_supported(a) ? ssm::scan_fast_workspace_bytes(a) : 0;
+    return a.seqlen > kShortSeq && ssm::scan_fast_supported(a) ? ssm::scan_fast_workspace_bytes(a) : 0;
 }
 
 ssm_status_t cuda_fail(cudaError_t e) {
@@ -228,8 +232,10 @@ ssm_status_t ssm_scan_fwd(const ssm_scan_params* p, void* stream) {
         return fail(SSM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
-    if ((a.debug_flags & SSM_DEBUG_SKIP_FIRST_LOAD) && (a.seqlen < 1 || a.seqlen > 16 || !ssm::scan_fast_supported(a)))
-        return fail(SSM_ERR_INVALID_ARG, "SSM_DEBUG_SKIP_FIRST_LOAD needs 1 <= seqlen <= 16 and the TMA path");
+    if ((a.debug_flags & SSM_DEBUG_SKIP_FIRST_LOAD) &&
+        (a.seqlen <= kShortSeq || a.seqlen > 16 || !ssm::scan_fast_supported(a)))
+        return fail(SSM_ERR_INVALID_ARG, "SSM_DEBUG_SKIP_FIRST_LOAD needs %lld < seqlen <= 16 and the TMA path",
+                    (long long)kShortSeq);
     if (a.seqlen == 0) {
         if (a.h_last) {
             const size_t bytes = (size_t)(a.batch * a.dim * a.dstate) * sizeof(float);
@@ -237,7 +243,7 @@ ssm_status_t ssm_scan_fwd(const ssm_scan_params* p, void* stream) {
                                          : cudaMemcpyAsync(a.h_last, a.h0, bytes, cudaMemcpyDeviceToDevice, st))
                      : cudaMemsetAsync(a.h_last, 0, bytes, st);
         }
-    } else if (ssm::scan_fast_supported(a)) {
+    } else if (a.seqlen > kShortSeq && ssm::scan_fast_supported(a)) {
         e = ssm::launch_scan_fast(a, st);
     } else {
         e = ssm::launch_scan_generic(a, st);

@@ -191,3 +191,39 @@ def test_invalid_args_raise_without_launch(cuda_dev):
     with pytest.raises(binding.SSMError) as e:
         ssm_scan_fwd(**inp2)
     assert e.value.status == binding.SSM_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("slices", [1, 3, 8])
+def test_host_entry_point_pipelines_rows_and_matches_device_call(cuda_dev, slices):
+    """ssm_scan_fwd_host splits the batch into row groups whose copies and scans overlap on
+    three streams; the rows are independent, so the result equals the one-call device scan."""
+    inp = make_scan_inputs(8, 300, 64, 16, "bf16", seed=321)
+    host = {k: (v.pin_memory() if v is not None else None) for k, v in inp.items()}
+    y_ref, h_ref = ssm_scan_fwd(**_to(cuda_dev, inp))
+    torch.cuda.synchronize()
+    cache = {}
+    for _ in range(2):
+        y, h = binding.ssm_scan_fwd_host(host, device=cuda_dev, dev_buffers=cache, slices=slices)
+        assert torch.equal(y, y_ref.cpu())
+        assert torch.equal(h, h_ref.cpu())
+
+
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_decode_steps_advance_the_state_in_place(cuda_dev, dt):
+    """Single-token recurrent inference: T calls with L = 1 and h0 = h_last = one state buffer
+    give the same outputs and final state as one scan over the T tokens."""
+    T = 24
+    inp = make_scan_inputs(2, T, 48, 16, dt, seed=2024, d_skip="normal")
+    h0 = torch.randn(2, 48, 16, generator=torch.Generator().manual_seed(7))
+    g = _to(cuda_dev, inp)
+    state = h0.to(cuda_dev).clone()
+    ys = []
+    for t in range(T):
+        step = {k: (v[:, t:t + 1] if k in ("x", "delta", "B", "C", "z") else v) for k, v in g.items()}
+        y, h = ssm_scan_fwd(**step, h0=state, h_last=state)
+        assert h.data_ptr() == state.data_ptr()
+        ys.append(y)
+    torch.cuda.synchronize()
+    y_ref, h_ref = oracle.ssm_scan_ref(**inp, h0=h0)
+    assert rel_l2(torch.cat(ys, 1).float().cpu().numpy(), y_ref) <= TOL_Y[dt]
+    assert rel_l2(state.cpu().numpy(), h_ref) <= TOL_H[dt]
