@@ -1,16 +1,17 @@
 // Mamba-2 SSD chunked scan on the fifth-generation tensor cores (tcgen05), for bf16 I/O with
 // head dimension P = 64 and state size N = 128.
 //
-// One CTA (256 threads) per (batch, head) walks the sequence in blocks of Q = 128 steps;
-// the N x P state S stays on chip (fp32 registers, two threads per row n, plus a bf16 copy
-// in shared memory as an MMA operand). Per block, with cum_t the inclusive cumulative sum of
-// dt A_h inside the block (the decay from the block start to step t):
+// One CTA per (batch, head) walks the sequence in blocks of Q = 128 steps; the N x P state S
+// stays on chip (fp32 registers, two threads per row n, plus a bf16 copy in shared memory as
+// an MMA operand). Per block, with cum_t the inclusive cumulative sum of dt A_h inside the
+// block (the decay from the block start to step t):
 //
 //   G      = C B^T                                  (Q x Q, K = N)      tcgen05, TMEM
 //   M[t,s] = G[t,s] exp(cum_t - cum_s) dt_s, s <= t; 0 above the diagonal
-//   Y      = M X + (exp(cum) o C) S_prev           (Q x P, K = Q + N)  tcgen05, M from TMEM
-//   y_t    = Y_t (+ D x_t) (* silu z_t)
-//   S      = exp(cum_last) S_prev + (w o B)^T X,    w_s = exp(cum_last - cum_s) dt_s
+//   Y      = M X                                    (Q x P, K = Q)      tcgen05, M from TMEM
+//   Yoff   = C S_prev                               (Q x P, K = N)      tcgen05
+//   y_t    = Y_t + exp(cum_t) Yoff_t  (+ D x_t) (* silu z_t)
+//   S      = exp(cum_last) S_prev + B^T (w o X),    w_s = exp(cum_last - cum_s) dt_s
 //                                                   (N x P, K = Q)      tcgen05
 //
 // which is the block decomposition of the semiseparable matrix of the recurrence
@@ -19,16 +20,22 @@
 // A chunk of Q' = 128 k steps (the chunk length the caller asks for) is computed as k such
 // blocks; the result does not depend on the chunk length beyond rounding.
 //
-// Data movement: TMA (4-D maps, 128-byte swizzle) brings the C and B blocks (128 x 128) and
-// the x block (128 x 64) into shared memory in the layouts the MMAs read directly (C and B
-// K-major for G; C, rescaled in place by exp(cum_t), K-major for the hand-off; B, rescaled
-// in place by w_s, as the MN-major A operand of the state product; x MN-major as the B
-// operand); the y block leaves by TMA store from the x buffer. The next block's C and B are
-// requested as soon as this block's products are done with them, its x once y has left.
-// Tensor memory: G (128 columns, then the state product), M in bf16 (64) and Y (64): 256
-// columns, so two CTAs share an SM. Eight warps: two per TMEM lane quarter (the rows a warp
-// may access), splitting the columns of the mask, scaling and epilogue work between them.
-// One thread issues the MMAs and waits for them; the others wait at the CTA barrier.
+// Pipeline. A control warp issues the TMA loads, the MMAs and the y stores; eight math warps
+// (two per TMEM lane quarter, splitting the columns) run the block scan of dt A, the mask,
+// the scaled copy w o X and the epilogue. Below the diagonal the mask's decay is factored per
+// 32-step chunk, exp(cum_t - cum_s) = exp(cum_t - cum_ref) exp(cum_ref - cum_s) with cum_ref
+// the chunk's last step (both factors <= 1), so those elements need no exponential. Tensor memory (all 512 columns) holds G twice, M,
+// Y, Yoff and the state product, and shared memory holds C, B and x twice, so that:
+//   * G of block j+1 is computed while the math warps mask block j,
+//   * Yoff of block j is computed as soon as the state S_{j-1} is written,
+//   * C, B and x of later blocks are loaded while the current ones are worked on.
+// Hand-offs go through mbarriers (tcgen05.commit for the MMAs, TMA transaction counts for
+// the loads, one elected arrival per phase of the math warps); every wait is bounded.
+//
+// Data layouts: TMA (4-D maps, 128-byte swizzle) brings C and B blocks (128 x 128) and x blocks
+// (128 x 64) into shared memory in the canonical layouts the MMAs read directly (C and B
+// K-major for G and Yoff; B as the MN-major A operand of the state product; x, w o x and the
+// bf16 state MN-major as B operands). y is staged in the x buffer of its block.
 //
 // Pages: "Mamba-2 / Structured State Space Duality" (abeam) "基本アイデア" (SSM as a
 // semiseparable matrix; diagonal blocks by ordinary matrix products, off-diagonal blocks by a
@@ -49,29 +56,32 @@ namespace {
 constexpr int kQ = 128;          // steps per block
 constexpr int kP = 64;           // head dimension
 constexpr int kN = 128;          // state size
-constexpr int kThreads = 256;    // 8 warps: two per TMEM lane quarter, splitting the columns
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColG = 0;    // G (128 columns); after the mask pass the state product (0..63)
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColM = 128;  // M in bf16 pairs (64 columns)
-constexpr uint32_t kColY = 192;  // Y = M X + (exp(cum) o C) S_prev (64 columns)
+constexpr int kMath = 256;       // 8 math warps
+constexpr int kThreads = kMath + 32;   // + the control warp
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColG = 0;    // G, two buffers of 128 columns
+constexpr uint32_t kColM = 256;  // M in bf16 pairs (64 columns)
+constexpr uint32_t kColY = 320;
+constexpr uint32_t kColYoff = 384;
+constexpr uint32_t kColS = 448;  // the state product
 
 constexpr int kAtom = 16384;     // 128 rows x 128 bytes
-constexpr int kSmC = 0;
-constexpr int kSmB = 2 * kAtom;
-constexpr int kSmX = 4 * kAtom;
-constexpr int kSmS = 5 * kAtom;
-constexpr int kSmCs = 6 * kAtom;             // float [kQ]: cum_t log2(e)
-constexpr int kSmLw = kSmCs + kQ * 4;        // float [kQ]: dt_s
-constexpr int kSmEv = kSmLw + kQ * 4;        // float [kQ]: exp(cum_t)
-constexpr int kSmWv = kSmEv + kQ * 4;        // float [kQ]: exp(cum_last - cum_s) dt_s
-constexpr int kSmRed = kSmWv + kQ * 4;       // float [8]: warp totals of the scan, exp(cum_last)
-constexpr int kSmBar = kSmRed + 64;          // 4 mbarriers: C, B and x loads, MMA completion
-constexpr int kSmTmem = kSmBar + 32;         // tensor-memory base address
-constexpr int kSmemUsed = kSmTmem + 16;
-constexpr int kSmemBytes = kSmemUsed + 1024; // room to align the base to 1024 bytes
+constexpr int kSmC = 0;                       // C, 2 stages x 2 atoms
+constexpr int kSmB = kSmC + 4 * kAtom;        // B, 2 stages x 2 atoms
+constexpr int kSmXw = kSmB + 4 * kAtom;       // w o x, 1 atom
+constexpr int kSmX = kSmXw + kAtom;           // x (then y), 2 stages
+constexpr int kSmS = kSmX + 2 * kAtom;        // bf16 state
+constexpr int kSmArr = kSmS + kAtom;          // per block (2 buffers): cs, dt, e, w, v, each float[kQ]
+constexpr int kNArr = 5;
+constexpr int kSmRed = kSmArr + 2 * kNArr * kQ * 4;   // float[8]
+constexpr int kSmBar = kSmRed + 64;           // 10 mbarriers
+constexpr int kSmTmem = kSmBar + 10 * 8;
+constexpr int kSmFlag = kSmTmem + 8;
+constexpr int kSmemUsed = kSmFlag + 8;
+constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024 bytes
 
 constexpr uint32_t kIdescG = tc::idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescYoff = tc::idesc_bf16(128, 64, false, true);
 constexpr uint32_t kIdescY = tc::idesc_bf16(128, 64, false, true);
 constexpr uint32_t kIdescS = tc::idesc_bf16(128, 64, true, true);
 
@@ -131,366 +141,414 @@ __device__ __forceinline__ uint4 scale_bf16x8(uint4 v, f2 s2) {
     return r;
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__device__ __forceinline__ uint4 pack8(const float* v) {
+    uint4 r;
+    r.x = tc::pack_bf16(v[0], v[1]);
+    r.y = tc::pack_bf16(v[2], v[3]);
+    r.z = tc::pack_bf16(v[4], v[5]);
+    r.w = tc::pack_bf16(v[6], v[7]);
+    return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
 ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CUtensorMap mB,
               const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap mY, const TcParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                          ~static_cast<uintptr_t>(1023));
-    unsigned char* sC = sm + kSmC;
-    unsigned char* sB = sm + kSmB;
-    unsigned char* sX = sm + kSmX;
-    unsigned char* sS = sm + kSmS;
-    float* cs = reinterpret_cast<float*>(sm + kSmCs);    // cum_t log2 e
-    float* lw = reinterpret_cast<float*>(sm + kSmLw);    // dt_s
-    float* ev = reinterpret_cast<float*>(sm + kSmEv);    // exp(cum_t)
-    float* wv = reinterpret_cast<float*>(sm + kSmWv);    // exp(cum_last - cum_s) dt_s
     float* red = reinterpret_cast<float*>(sm + kSmRed);
-    uint64_t* bar_c = reinterpret_cast<uint64_t*>(sm + kSmBar);
-    uint64_t* bar_b = bar_c + 1;
-    uint64_t* bar_x = bar_c + 2;
-    uint64_t* bar_mma = bar_c + 3;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSmBar);
+    uint64_t* full_cb = bars + 0;      // [2] C and B of a stage loaded
+    uint64_t* full_x = bars + 2;       // [2] x of a stage loaded
+    uint64_t* g_done = bars + 4;       // [2] G of a buffer computed
+    uint64_t* yoff_done = bars + 6;    // Yoff of the block computed (all earlier MMAs too)
+    uint64_t* mma2_done = bars + 7;    // Y and the state product computed
+    uint64_t* math_ready = bars + 8;   // M and w o X of the block written
+    uint64_t* epi_done = bars + 9;     // state and y of the block written, accumulators read
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kSmTmem);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kSmFlag);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3;        // the TMEM lanes (rows) this warp can access
-    const int half = warp >> 2;          // which half of the columns (or atom) it takes
-    const int row = tid & 127;           // = 32 quarter + lane
     const int h = blockIdx.x, b = blockIdx.y;
     const int grp = h / p.heads_per_group;
     const int64_t L = p.seqlen;
     const int H = p.nheads;
+    const int nblk = p.nblocks;
 
     if (warp == 0) tc::tmem_alloc(tslot, kTmemCols);
-    if (tid == 0) {
-        mbar_init(bar_c, 1);
-        mbar_init(bar_b, 1);
-        mbar_init(bar_x, 1);
-        mbar_init(bar_mma, 1);
+    if (tid == kMath) {
+        for (int i = 0; i < 10; ++i) mbar_init(&bars[i], 1);
+        *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&mX);
         prefetch_tensormap(&mB);
         prefetch_tensormap(&mC);
         prefetch_tensormap(&mY);
     }
-
-    // the state: row `row`, columns [32 half, 32 half + 32) in fp32 registers; its bf16 copy
-    // (the B operand of the hand-off product) in sS
-    float S[kP / 2];
-    {
-        const float* src = p.h0 ? p.h0 + (((int64_t)b * H + h) * kN + row) * kP + 32 * half : nullptr;
-#pragma unroll
-        for (int i = 0; i < kP / 2; i += 4) {
-            const float4 v = src ? *reinterpret_cast<const float4*>(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-            S[i] = v.x;
-            S[i + 1] = v.y;
-            S[i + 2] = v.z;
-            S[i + 3] = v.w;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint4 v;
-            v.x = tc::pack_bf16(S[8 * j], S[8 * j + 1]);
-            v.y = tc::pack_bf16(S[8 * j + 2], S[8 * j + 3]);
-            v.z = tc::pack_bf16(S[8 * j + 4], S[8 * j + 5]);
-            v.w = tc::pack_bf16(S[8 * j + 6], S[8 * j + 7]);
-            *reinterpret_cast<uint4*>(sS + sw128(row, 4 * half + j)) = v;
-        }
-    }
-    fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tslot;
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
 
-    const float Ah = p.A[h];
-    const float bias = p.bias ? p.bias[h] : 0.f;
-    const float Dh = p.D ? p.D[h] : 0.f;
-    const uint32_t aC = smem_u32(sC), aB = smem_u32(sB), aX = smem_u32(sX), aS = smem_u32(sS);
-    const __nv_bfloat16* delta = static_cast<const __nv_bfloat16*>(p.delta);
-
-    // Load schedule: C and B of block j+1 once the products of block j are done with them,
-    // x of block j+1 once the y of block j (staged in the x buffer) has been read out by its
-    // TMA store.
-    auto load_c = [&](int j) {
-        mbar_arrive_expect_tx(bar_c, 2 * kAtom);
-        tma_load_4d(sC, &mC, 0, grp, j * kQ, b, bar_c);
-        tma_load_4d(sC + kAtom, &mC, 64, grp, j * kQ, b, bar_c);
-    };
-    auto load_b = [&](int j) {
-        mbar_arrive_expect_tx(bar_b, 2 * kAtom);
-        tma_load_4d(sB, &mB, 0, grp, j * kQ, b, bar_b);
-        tma_load_4d(sB + kAtom, &mB, 64, grp, j * kQ, b, bar_b);
-    };
-    auto load_x = [&](int j) {
-        mbar_arrive_expect_tx(bar_x, kAtom);
-        tma_load_4d(sX, &mX, 0, h, j * kQ, b, bar_x);
-    };
-    if (tid == 0 && p.nblocks > 0) {
-        load_c(0);
-        load_b(0);
-        load_x(0);
-    }
-    // delta of row t (threads of the first warpgroup), one block ahead
-    auto load_delta = [&](int j) -> float {
-        const int64_t tt = (int64_t)j * kQ + row;
-        return (half == 0 && j < p.nblocks && tt < L) ? __bfloat162float(delta[((int64_t)b * L + tt) * H + h]) : 0.f;
-    };
-    float draw_next = load_delta(0);
-
-    unsigned ph_mma = 0;
-    bool failed = false;
-    for (int j = 0; j < p.nblocks; ++j) {
-        const int t0 = j * kQ;
-        const unsigned ph_ld = j & 1;
-        const int64_t t = t0 + row;
-        // dt_t and the inclusive cumulative sum of dt A_h over the block (first warpgroup, row t)
-        if (half == 0) {
-            float dt = 0.f;
-            if (t < L) {
-                const float v = draw_next + bias;
-                dt = p.softplus ? softplus_accurate(v) : v;
-            }
-            float cum = dt * Ah;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float n = __shfl_up_sync(0xffffffffu, cum, o);
-                if (lane >= o) cum += n;
-            }
-            if (lane == 31) red[warp] = cum;
-            cs[row] = cum;   // provisional: the warp-local prefix, completed below
-            lw[row] = dt;
-        }
-        draw_next = load_delta(j + 1);
-        __syncthreads();
-        if (half == 0) {
-            float before = 0.f;
-#pragma unroll
-            for (int w = 0; w < 4; ++w)
-                if (w < warp) before += red[w];
-            const float cum = cs[row] + before;
-            const float dt = lw[row];
-            const float cum_last = red[0] + red[1] + red[2] + red[3];
-            const float cs_t = cum * kLog2e;
-            cs[row] = cs_t;
-            lw[row] = dt;
-            ev[row] = ex2_approx(cs_t);
-            wv[row] = ex2_approx((cum_last - cum) * kLog2e) * dt;
-            if (row == 0) red[4] = ex2_approx(cum_last * kLog2e);
-        }
-
-        // G = C B^T (one thread issues and waits; the others wait at the barrier)
-        bool ok = true;
-        if (tid == 0) {
-            ok = mbar_wait_bounded(bar_c, ph_ld, p.status) && mbar_wait_bounded(bar_b, ph_ld, p.status);
-            if (ok) {
-                tc::fence_after_sync();
+    if (warp == kMath / 32) {
+        // ============================ control warp (one lane) ============================
+        if (lane == 0) {
+            const uint32_t aS = smem_u32(sm + kSmS), aXw = smem_u32(sm + kSmXw);
+            auto aC = [&](int s) { return smem_u32(sm + kSmC + s * 2 * kAtom); };
+            auto aB = [&](int s) { return smem_u32(sm + kSmB + s * 2 * kAtom); };
+            auto aX = [&](int s) { return smem_u32(sm + kSmX + s * kAtom); };
+            auto load_cb = [&](int j) {
+                const int s = j & 1;
+                mbar_arrive_expect_tx(&full_cb[s], 4 * kAtom);
+                tma_load_4d(sm + kSmC + s * 2 * kAtom, &mC, 0, grp, j * kQ, b, &full_cb[s]);
+                tma_load_4d(sm + kSmC + s * 2 * kAtom + kAtom, &mC, 64, grp, j * kQ, b, &full_cb[s]);
+                tma_load_4d(sm + kSmB + s * 2 * kAtom, &mB, 0, grp, j * kQ, b, &full_cb[s]);
+                tma_load_4d(sm + kSmB + s * 2 * kAtom + kAtom, &mB, 64, grp, j * kQ, b, &full_cb[s]);
+            };
+            auto load_x = [&](int j) {
+                const int s = j & 1;
+                mbar_arrive_expect_tx(&full_x[s], kAtom);
+                tma_load_4d(sm + kSmX + s * kAtom, &mX, 0, h, j * kQ, b, &full_x[s]);
+            };
+            auto issue_g = [&](int j) {
+                const int s = j & 1;
 #pragma unroll
                 for (int k = 0; k < kN / 16; ++k) {
                     const uint32_t off = (k / 4) * kAtom + (k % 4) * 32;
-                    tc::mma_ss(tmem + kColG, tc::sdesc_sw128(aC + off, 16, 1024),
-                               tc::sdesc_sw128(aB + off, 16, 1024), kIdescG, k > 0);
+                    tc::mma_ss(tmem + kColG + 128 * s, tc::sdesc_sw128(aC(s) + off, 16, 1024),
+                               tc::sdesc_sw128(aB(s) + off, 16, 1024), kIdescG, k > 0);
                 }
-                tc::commit(bar_mma);
-                ok = mbar_wait_bounded(bar_mma, ph_mma, p.status);
-            }
-        }
-        ph_mma ^= 1;
-        if (__syncthreads_or(!ok)) {
-            failed = true;
-            break;
-        }
-        tc::fence_after_sync();
-        const float cs_t = cs[row];
-        const float e_last = red[4];
-
-        // G has read C and B: scale them in place, row t of C by exp(cum_t) (the decay from the
-        // block start, so that (exp(cum) o C) S_prev is the state hand-off) and row s of B by
-        // w_s = exp(cum_last - cum_s) dt_s (the weights of the state product (w o B)^T X).
-        // Thread (row, half) takes atom `half` of the row; the chunks are walked in swizzled
-        // order so that eight consecutive rows hit eight different bank groups.
-        {
-            const f2 e2 = pk(ev[row], ev[row]);
-            const f2 w2 = pk(wv[row], wv[row]);
-            uint4* rowc = reinterpret_cast<uint4*>(sC + half * kAtom + row * 128);
-            uint4* rowb = reinterpret_cast<uint4*>(sB + half * kAtom + row * 128);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int c = i ^ (row & 7);
-                rowc[c] = scale_bf16x8(rowc[c], e2);
-                rowb[c] = scale_bf16x8(rowb[c], w2);
-            }
-        }
-        // M[t, s] = G[t, s] exp(cum_t - cum_s) dt_s for s <= t (bf16 pairs in columns kColM..):
-        // warp (quarter, half) takes the 32-column chunks kc = half and half + 2 of its rows
-#pragma unroll
-        for (int ic = 0; ic < 2; ++ic) {
-            const int kc = half + 2 * ic;
-            uint32_t packed[16];
-            if (kc < quarter) {          // below the diagonal: every s < t
-                uint32_t r[32];
-                tc::ld32(lane_base + kColG + 32 * kc, r);
-                tc::wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 c4 = *reinterpret_cast<const float4*>(cs + 32 * kc + i);
-                    const float4 d4 = *reinterpret_cast<const float4*>(lw + 32 * kc + i);
-                    packed[i / 2] = tc::pack_bf16(__uint_as_float(r[i]) * d4.x * ex2_approx(cs_t - c4.x),
-                                                  __uint_as_float(r[i + 1]) * d4.y * ex2_approx(cs_t - c4.y));
-                    packed[i / 2 + 1] = tc::pack_bf16(__uint_as_float(r[i + 2]) * d4.z * ex2_approx(cs_t - c4.z),
-                                                      __uint_as_float(r[i + 3]) * d4.w * ex2_approx(cs_t - c4.w));
+                tc::commit(&g_done[s]);
+            };
+            bool ok = true;
+            auto wait = [&](uint64_t* bar, unsigned parity) {
+                if (ok && !mbar_wait_bounded(bar, parity, p.status)) ok = false;
+                return ok;
+            };
+            if (nblk > 0) {
+                load_cb(0);
+                load_x(0);
+                if (nblk > 1) {
+                    load_cb(1);
+                    load_x(1);
                 }
-            } else if (kc == quarter) {  // the diagonal chunk: s <= t
-                uint32_t r[32];
-                tc::ld32(lane_base + kColG + 32 * kc, r);
-                tc::wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 c4 = *reinterpret_cast<const float4*>(cs + 32 * kc + i);
-                    const float4 d4 = *reinterpret_cast<const float4*>(lw + 32 * kc + i);
-                    const float m0 = i <= lane ? __uint_as_float(r[i]) * d4.x * ex2_approx(cs_t - c4.x) : 0.f;
-                    const float m1 = i + 1 <= lane ? __uint_as_float(r[i + 1]) * d4.y * ex2_approx(cs_t - c4.y) : 0.f;
-                    const float m2 = i + 2 <= lane ? __uint_as_float(r[i + 2]) * d4.z * ex2_approx(cs_t - c4.z) : 0.f;
-                    const float m3 = i + 3 <= lane ? __uint_as_float(r[i + 3]) * d4.w * ex2_approx(cs_t - c4.w) : 0.f;
-                    packed[i / 2] = tc::pack_bf16(m0, m1);
-                    packed[i / 2 + 1] = tc::pack_bf16(m2, m3);
+                if (wait(&full_cb[0], 0)) {
+                    tc::fence_after_sync();
+                    issue_g(0);
                 }
-            } else {                     // above the diagonal
-#pragma unroll
-                for (int i = 0; i < 16; ++i) packed[i] = 0u;
             }
-            tc::st16(lane_base + kColM + 16 * kc, packed);
-        }
-        tc::wait_st();
-        fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        // Y = M X + (exp(cum) o C) S_prev and S_acc = (w o B)^T X (S_acc over G's columns)
-        if (tid == 0) {
-            ok = mbar_wait_bounded(bar_x, ph_ld, p.status);
-            if (ok) {
+            for (int j = 0; j < nblk && ok; ++j) {
+                const int s = j & 1;
+                // the state S_{j-1} is written and the accumulators of block j-1 are read
+                if (!wait(epi_done, j & 1)) break;
+                tc::fence_after_sync();
+                if (j > 0) {
+                    // y of block j-1 (staged in its x buffer) leaves; that buffer takes x_{j+1}
+                    // once the store has read it (below, after this block's products are issued)
+                    tma_store_4d(&mY, 0, h, (j - 1) * kQ, b, sm + kSmX + (s ^ 1) * kAtom);
+                    tma_store_commit();
+                }
+                // Yoff_j = C_j S_{j-1}
+#pragma unroll
+                for (int k = 0; k < kN / 16; ++k) {
+                    const uint32_t off = (k / 4) * kAtom + (k % 4) * 32;
+                    tc::mma_ss(tmem + kColYoff, tc::sdesc_sw128(aC(s) + off, 16, 1024),
+                               tc::sdesc_sw128(aS + k * 2048, kAtom, 1024), kIdescYoff, k > 0);
+                }
+                tc::commit(yoff_done);
+                // G_{j+1} into the other buffer (its previous contents, G_{j-1}, were masked
+                // before block j-1's products were issued)
+                if (j + 1 < nblk) {
+                    if (!wait(&full_cb[s ^ 1], ((j + 1) >> 1) & 1)) break;
+                    tc::fence_after_sync();
+                    issue_g(j + 1);
+                }
+                // Y_j = M_j X_j and S_acc_j = B_j^T (w o X_j) once M_j and w o X_j are written
+                if (!wait(math_ready, j & 1) || !wait(&full_x[s], (j >> 1) & 1)) break;
                 tc::fence_after_sync();
 #pragma unroll
                 for (int k = 0; k < kQ / 16; ++k)
-                    tc::mma_ts(tmem + kColY, tmem + kColM + 8 * k, tc::sdesc_sw128(aX + k * 2048, kAtom, 1024),
+                    tc::mma_ts(tmem + kColY, tmem + kColM + 8 * k, tc::sdesc_sw128(aX(s) + k * 2048, kAtom, 1024),
                                kIdescY, k > 0);
 #pragma unroll
-                for (int k = 0; k < kN / 16; ++k) {
-                    const uint32_t off = (k / 4) * kAtom + (k % 4) * 32;
-                    tc::mma_ss(tmem + kColY, tc::sdesc_sw128(aC + off, 16, 1024),
-                               tc::sdesc_sw128(aS + k * 2048, kAtom, 1024), kIdescY, 1);
-                }
-#pragma unroll
                 for (int k = 0; k < kQ / 16; ++k)
-                    tc::mma_ss(tmem + kColS, tc::sdesc_sw128(aB + k * 2048, kAtom, 1024),
-                               tc::sdesc_sw128(aX + k * 2048, kAtom, 1024), kIdescS, k > 0);
-                tc::commit(bar_mma);
-                ok = mbar_wait_bounded(bar_mma, ph_mma, p.status);
+                    tc::mma_ss(tmem + kColS, tc::sdesc_sw128(aB(s) + k * 2048, kAtom, 1024),
+                               tc::sdesc_sw128(aXw + k * 2048, kAtom, 1024), kIdescS, k > 0);
+                tc::commit(mma2_done);
+                if (j > 0 && j + 1 < nblk) {
+                    tma_store_wait_read<0>();   // y of block j-1 has left x buffer s ^ 1
+                    load_x(j + 1);
+                }
+                // C_j and B_j are free once the products of block j are done: stage s takes
+                // block j+2
+                if (j + 2 < nblk) {
+                    if (!wait(mma2_done, j & 1)) break;
+                    load_cb(j + 2);
+                }
             }
-            // C and B of this block are no longer read
-            if (ok && j + 1 < p.nblocks) {
-                load_c(j + 1);
-                load_b(j + 1);
+            if (ok && nblk > 0) {
+                // the last y
+                if (wait(epi_done, nblk & 1)) {
+                    tma_store_4d(&mY, 0, h, (nblk - 1) * kQ, b, sm + kSmX + ((nblk - 1) & 1) * kAtom);
+                    tma_store_commit();
+                }
             }
+            tma_store_wait_all();
+            if (!ok) *abort_flag = 1;
         }
-        ph_mma ^= 1;
-        if (__syncthreads_or(!ok)) {
-            failed = true;
-            break;
-        }
-        tc::fence_after_sync();
+    } else {
+        // ============================ math warps ============================
+        const int quarter = warp & 3;        // the TMEM lanes (rows) this warp can access
+        const int half = warp >> 2;          // which half of the columns (or atom) it takes
+        const int row = tid & 127;           // = 32 quarter + lane
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * quarter) << 16);
+        const float Ah = p.A[h];
+        const float bias = p.bias ? p.bias[h] : 0.f;
+        const float Dh = p.D ? p.D[h] : 0.f;
+        const __nv_bfloat16* delta = static_cast<const __nv_bfloat16*>(p.delta);
+        auto arr = [&](int buf, int which) {
+            return reinterpret_cast<float*>(sm + kSmArr) + (buf * kNArr + which) * kQ;
+        };
+        // a bounded wait whose outcome is the same for the whole warp (the warp-collective
+        // tensor-memory accesses that follow must be taken by all its lanes or none)
+        auto wait_warp = [&](uint64_t* bar, unsigned parity) {
+            const bool okl = mbar_wait_bounded(bar, parity, p.status);
+            return __all_sync(0xffffffffu, okl) != 0;
+        };
+        // all math threads done with a phase: one arrival; false if any thread failed
+        auto signal = [&](uint64_t* bar, bool okt) -> bool {
+            const bool bad = named_bar_or(1, kMath, !okt || *abort_flag);
+            if (tid == 0) mbar_arrive(bar);
+            return !bad;
+        };
+        auto load_delta = [&](int j) -> float {
+            const int64_t tt = (int64_t)j * kQ + row;
+            return (half == 0 && j < nblk && tt < L) ? __bfloat162float(delta[((int64_t)b * L + tt) * H + h]) : 0.f;
+        };
+        // the block scan of dt A_h for block j into array buffer j & 1 (first warpgroup)
+        auto scan_block = [&](int j, float draw) {
+            const int buf = j & 1;
+            float dt = 0.f, cum = 0.f;
+            if (half == 0) {
+                if ((int64_t)j * kQ + row < L) {
+                    const float v = draw + bias;
+                    dt = p.softplus ? softplus_accurate(v) : v;
+                }
+                cum = dt * Ah;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float n = __shfl_up_sync(0xffffffffu, cum, o);
+                    if (lane >= o) cum += n;
+                }
+                if (lane == 31) red[warp] = cum;
+            }
+            named_bar_or(1, kMath, false);
+            if (half == 0) {
+                float before = 0.f;
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    if (w < warp) before += red[w];
+                cum += before;
+                const float cum_last = red[0] + red[1] + red[2] + red[3];
+                const float cs_t = cum * kLog2e;
+                arr(buf, 0)[row] = cs_t;
+                arr(buf, 1)[row] = dt;
+                arr(buf, 2)[row] = ex2_approx(cs_t);
+                arr(buf, 3)[row] = ex2_approx((cum_last - cum) * kLog2e) * dt;
+                // v_s = dt_s exp(cum_ref - cum_s), cum_ref the cumulative sum at the last step of
+                // the 32-step chunk of s (this warp's lane 31): cum_ref <= cum_s, so v_s <= dt_s
+                const float cs_ref = __shfl_sync(0xffffffffu, cs_t, 31);
+                arr(buf, 4)[row] = dt * ex2_approx(cs_ref - cs_t);
+                if (row == 0) red[4 + buf] = ex2_approx(cum_last * kLog2e);
+            }
+            named_bar_or(1, kMath, false);
+        };
 
-        // epilogue: y row t, columns [32 half, +32) into sX (free now); the state row, same
-        // columns; 16 columns at a time
-        const __nv_bfloat16* xrow = p.D && t < L ? static_cast<const __nv_bfloat16*>(p.x) +
-                                                       (((int64_t)b * L + t) * H + h) * kP + 32 * half
-                                                 : nullptr;
-        const __nv_bfloat16* zrow = p.z && t < L ? static_cast<const __nv_bfloat16*>(p.z) +
-                                                       (((int64_t)b * L + t) * H + h) * kP + 32 * half
-                                                 : nullptr;
+        // initial state: row `row`, columns [32 half, +32) in registers, bf16 copy in sS
+        float S[kP / 2];
+        {
+            const float* src = p.h0 ? p.h0 + (((int64_t)b * H + h) * kN + row) * kP + 32 * half : nullptr;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            uint32_t ry[16];
-            tc::ld16(lane_base + kColY + 32 * half + 16 * q, ry);
-            tc::wait_ld();
-            float yv[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) yv[i] = __uint_as_float(ry[i]);
-            if (xrow) {
-#pragma unroll
-                for (int i = 0; i < 16; i += 8) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(xrow + 16 * q + i);
-                    yv[i] = fmaf(Dh, bf_lo(v.x), yv[i]);
-                    yv[i + 1] = fmaf(Dh, bf_hi(v.x), yv[i + 1]);
-                    yv[i + 2] = fmaf(Dh, bf_lo(v.y), yv[i + 2]);
-                    yv[i + 3] = fmaf(Dh, bf_hi(v.y), yv[i + 3]);
-                    yv[i + 4] = fmaf(Dh, bf_lo(v.z), yv[i + 4]);
-                    yv[i + 5] = fmaf(Dh, bf_hi(v.z), yv[i + 5]);
-                    yv[i + 6] = fmaf(Dh, bf_lo(v.w), yv[i + 6]);
-                    yv[i + 7] = fmaf(Dh, bf_hi(v.w), yv[i + 7]);
-                }
-            }
-            if (zrow) {
-#pragma unroll
-                for (int i = 0; i < 16; i += 8) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(zrow + 16 * q + i);
-                    yv[i] *= silu_accurate(bf_lo(v.x));
-                    yv[i + 1] *= silu_accurate(bf_hi(v.x));
-                    yv[i + 2] *= silu_accurate(bf_lo(v.y));
-                    yv[i + 3] *= silu_accurate(bf_hi(v.y));
-                    yv[i + 4] *= silu_accurate(bf_lo(v.z));
-                    yv[i + 5] *= silu_accurate(bf_hi(v.z));
-                    yv[i + 6] *= silu_accurate(bf_lo(v.w));
-                    yv[i + 7] *= silu_accurate(bf_hi(v.w));
-                }
+            for (int i = 0; i < kP / 2; i += 4) {
+                const float4 v = src ? *reinterpret_cast<const float4*>(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                S[i] = v.x;
+                S[i + 1] = v.y;
+                S[i + 2] = v.z;
+                S[i + 3] = v.w;
             }
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint4 v;
-                v.x = tc::pack_bf16(yv[8 * c], yv[8 * c + 1]);
-                v.y = tc::pack_bf16(yv[8 * c + 2], yv[8 * c + 3]);
-                v.z = tc::pack_bf16(yv[8 * c + 4], yv[8 * c + 5]);
-                v.w = tc::pack_bf16(yv[8 * c + 6], yv[8 * c + 7]);
-                *reinterpret_cast<uint4*>(sX + sw128(row, 4 * half + 2 * q + c)) = v;
-            }
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(sm + kSmS + sw128(row, 4 * half + c)) = pack8(S + 8 * c);
         }
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            uint32_t rs[16];
-            tc::ld16(lane_base + kColS + 32 * half + 16 * q, rs);
-            tc::wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) S[16 * q + i] = fmaf(e_last, S[16 * q + i], __uint_as_float(rs[i]));
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint4 v;
-                v.x = tc::pack_bf16(S[16 * q + 8 * c], S[16 * q + 8 * c + 1]);
-                v.y = tc::pack_bf16(S[16 * q + 8 * c + 2], S[16 * q + 8 * c + 3]);
-                v.z = tc::pack_bf16(S[16 * q + 8 * c + 4], S[16 * q + 8 * c + 5]);
-                v.w = tc::pack_bf16(S[16 * q + 8 * c + 6], S[16 * q + 8 * c + 7]);
-                *reinterpret_cast<uint4*>(sS + sw128(row, 4 * half + 2 * q + c)) = v;
-            }
-        }
+        scan_block(0, load_delta(0));
         fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tma_store_4d(&mY, 0, h, t0, b, sX);
-            tma_store_commit();
-            if (j + 1 < p.nblocks) {
-                tma_store_wait_read<0>();   // y has left the x buffer
-                load_x(j + 1);
-            }
-        }
-    }
-    if (tid == 0) tma_store_wait_all();
-    if (!failed && p.h_last) {
-        float* dst = p.h_last + (((int64_t)b * H + h) * kN + row) * kP + 32 * half;
+        bool ok = signal(epi_done, true);    // the initial state is in place
+
+        for (int j = 0; j < nblk && ok; ++j) {
+            const int s = j & 1;
+            const float* cs = arr(s, 0);
+            const float* dts = arr(s, 1);
+            const float* vs = arr(s, 4);
+            // delta of block j+1: issued here, used after the mask (no barrier in between)
+            const float draw_next = load_delta(j + 1);
+            // ---- wait for x_j and G_j, and for block j-1's products to have consumed M and w o X
+            bool okw = wait_warp(&full_x[s], (j >> 1) & 1) && wait_warp(&g_done[s], (j >> 1) & 1);
+            if (okw && j > 0) okw = wait_warp(mma2_done, (j - 1) & 1);
+            tc::fence_after_sync();
+            if (okw) {
+                // ---- mask: M[t, s'] = G[t, s'] exp(cum_t - cum_s') dt_s' for s' <= t; warp
+                // (quarter, half) takes the 32-column chunks half and half + 2 of its rows
+                const float cs_t = cs[row];
 #pragma unroll
-        for (int i = 0; i < kP / 2; i += 4)
-            *reinterpret_cast<float4*>(dst + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
+                for (int ic = 0; ic < 2; ++ic) {
+                    const int kc = half + 2 * ic;
+                    uint32_t packed[16];
+                    if (kc <= quarter) {
+                        uint32_t r[32];
+                        tc::ld32(lane_base + kColG + 128 * s + 32 * kc, r);
+                        tc::wait_ld();
+                        if (kc < quarter) {
+                            // below the diagonal: exp(cum_t - cum_s) dt_s = f_t v_s with
+                            // f_t = exp(cum_t - cum_ref) <= 1 (t is past the chunk)
+                            const float f = ex2_approx(cs_t - cs[32 * kc + 31]);
+                            const f2 f2v = pk(f, f);
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4) {
+                                const ulonglong2 v4 = *reinterpret_cast<const ulonglong2*>(vs + 32 * kc + i);
+                                float m0, m1, m2, m3;
+                                upk(mul2(mul2(pk(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), v4.x), f2v), m0, m1);
+                                upk(mul2(mul2(pk(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])), v4.y), f2v), m2,
+                                    m3);
+                                packed[i / 2] = tc::pack_bf16(m0, m1);
+                                packed[i / 2 + 1] = tc::pack_bf16(m2, m3);
+                            }
+                        } else {
+                            // the diagonal chunk: s <= t, exp(cum_t - cum_s) directly
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4) {
+                                const float4 c4 = *reinterpret_cast<const float4*>(cs + 32 * kc + i);
+                                const float4 d4 = *reinterpret_cast<const float4*>(dts + 32 * kc + i);
+                                const float m0 = i <= lane ? __uint_as_float(r[i]) * d4.x * ex2_approx(cs_t - c4.x) : 0.f;
+                                const float m1 =
+                                    i + 1 <= lane ? __uint_as_float(r[i + 1]) * d4.y * ex2_approx(cs_t - c4.y) : 0.f;
+                                const float m2 =
+                                    i + 2 <= lane ? __uint_as_float(r[i + 2]) * d4.z * ex2_approx(cs_t - c4.z) : 0.f;
+                                const float m3 =
+                                    i + 3 <= lane ? __uint_as_float(r[i + 3]) * d4.w * ex2_approx(cs_t - c4.w) : 0.f;
+                                packed[i / 2] = tc::pack_bf16(m0, m1);
+                                packed[i / 2 + 1] = tc::pack_bf16(m2, m3);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) packed[i] = 0u;
+                    }
+                    tc::st16(lane_base + kColM + 16 * kc, packed);
+                }
+                // ---- w o X_j: thread tid takes row tid / 2, chunks 4 (tid & 1) .. + 3, walked so
+                // that the eight lanes of a shared-memory phase hit eight bank groups
+                {
+                    const int xr = tid >> 1, xg = tid & 1;
+                    const float wt = arr(s, 3)[xr];
+                    const f2 w2 = pk(wt, wt);
+                    const unsigned char* src = sm + kSmX + s * kAtom + xr * 128;
+                    unsigned char* dst = sm + kSmXw + xr * 128;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int c = (4 * xg + i) ^ (xr & 7);
+                        *reinterpret_cast<uint4*>(dst + 16 * c) =
+                            scale_bf16x8(*reinterpret_cast<const uint4*>(src + 16 * c), w2);
+                    }
+                }
+                tc::wait_st();
+            }
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            ok = signal(math_ready, okw);
+            if (!ok) break;
+
+            // ---- the scan of the next block while the tensor core works
+            if (j + 1 < nblk) scan_block(j + 1, draw_next);
+
+            // ---- epilogue: y row t (columns [32 half, +32)) into x buffer s, the state row
+            okw = wait_warp(mma2_done, j & 1) && wait_warp(yoff_done, j & 1);
+            tc::fence_after_sync();
+            if (okw) {
+                const int64_t t = (int64_t)j * kQ + row;
+                const float e_t = arr(s, 2)[row];
+                const float e_last = red[4 + s];
+                const __nv_bfloat16* xrow = p.D && t < L ? static_cast<const __nv_bfloat16*>(p.x) +
+                                                               (((int64_t)b * L + t) * H + h) * kP + 32 * half
+                                                         : nullptr;
+                const __nv_bfloat16* zrow = p.z && t < L ? static_cast<const __nv_bfloat16*>(p.z) +
+                                                               (((int64_t)b * L + t) * H + h) * kP + 32 * half
+                                                         : nullptr;
+                unsigned char* ys = sm + kSmX + s * kAtom;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t ry[16], ro[16];
+                    tc::ld16(lane_base + kColY + 32 * half + 16 * q, ry);
+                    tc::ld16(lane_base + kColYoff + 32 * half + 16 * q, ro);
+                    tc::wait_ld();
+                    float yv[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) yv[i] = fmaf(e_t, __uint_as_float(ro[i]), __uint_as_float(ry[i]));
+                    if (xrow) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 8) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(xrow + 16 * q + i);
+                            yv[i] = fmaf(Dh, bf_lo(v.x), yv[i]);
+                            yv[i + 1] = fmaf(Dh, bf_hi(v.x), yv[i + 1]);
+                            yv[i + 2] = fmaf(Dh, bf_lo(v.y), yv[i + 2]);
+                            yv[i + 3] = fmaf(Dh, bf_hi(v.y), yv[i + 3]);
+                            yv[i + 4] = fmaf(Dh, bf_lo(v.z), yv[i + 4]);
+                            yv[i + 5] = fmaf(Dh, bf_hi(v.z), yv[i + 5]);
+                            yv[i + 6] = fmaf(Dh, bf_lo(v.w), yv[i + 6]);
+                            yv[i + 7] = fmaf(Dh, bf_hi(v.w), yv[i + 7]);
+                        }
+                    }
+                    if (zrow) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 8) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(zrow + 16 * q + i);
+                            yv[i] *= silu_accurate(bf_lo(v.x));
+                            yv[i + 1] *= silu_accurate(bf_hi(v.x));
+                            yv[i + 2] *= silu_accurate(bf_lo(v.y));
+                            yv[i + 3] *= silu_accurate(bf_hi(v.y));
+                            yv[i + 4] *= silu_accurate(bf_lo(v.z));
+                            yv[i + 5] *= silu_accurate(bf_hi(v.z));
+                            yv[i + 6] *= silu_accurate(bf_lo(v.w));
+                            yv[i + 7] *= silu_accurate(bf_hi(v.w));
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        *reinterpret_cast<uint4*>(ys + sw128(row, 4 * half + 2 * q + c)) = pack8(yv + 8 * c);
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t rs[16];
+                    tc::ld16(lane_base + kColS + 32 * half + 16 * q, rs);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) S[16 * q + i] = fmaf(e_last, S[16 * q + i], __uint_as_float(rs[i]));
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        *reinterpret_cast<uint4*>(sm + kSmS + sw128(row, 4 * half + 2 * q + c)) =
+                            pack8(S + 16 * q + 8 * c);
+                }
+            }
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            ok = signal(epi_done, okw);
+        }
+        if (ok && p.h_last) {
+            float* dst = p.h_last + (((int64_t)b * H + h) * kN + row) * kP + 32 * half;
+#pragma unroll
+            for (int i = 0; i < kP / 2; i += 4)
+                *reinterpret_cast<float4*>(dst + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
+        }
     }
     tc::fence_before_sync();
     __syncthreads();

@@ -57,6 +57,23 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
     }
 }
 
+// One plain arrival on `bar` (no transaction bytes).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier among `count` threads (a multiple of 32) on named barrier `id` (not 0, which
+// __syncthreads uses); returns the OR of `pred` over those threads.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+    int r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n barrier.red.or.pred q, %2, %3, p;\n selp.b32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((int)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // 3-D tiled TMA load of the box at (c0, c1, c2) into shared memory; completion is counted
 // in bytes on `bar`.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
