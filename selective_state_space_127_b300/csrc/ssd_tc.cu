@@ -24,11 +24,17 @@
 // (two per TMEM lane quarter, splitting the columns) run the block scan of dt A, the mask,
 // the scaled copy w o X and the epilogue. Below the diagonal the mask's decay is factored per
 // 32-step chunk, exp(cum_t - cum_s) = exp(cum_t - cum_ref) exp(cum_ref - cum_s) with cum_ref
-// the chunk's last step (both factors <= 1), so those elements need no exponential. Tensor memory (all 512 columns) holds G twice, M,
-// Y, Yoff and the state product, and shared memory holds C, B and x twice, so that:
-//   * G of block j+1 is computed while the math warps mask block j,
+// the chunk's last step (both factors <= 1), so those elements need no exponential.
+// Only the state carries a dependence from block to block (through Yoff and the epilogue); the
+// mask and the products Y, S_acc of a block do not wait for the state. The math warps therefore
+// run one block apart: mask block j, then (while the tensor core computes Y_j and S_acc_j) the
+// epilogue of block j-1, then the scan of dt A for block j+1. Tensor memory holds G twice, M
+// and Yoff; once a G buffer is masked, Y (columns 0-63) and S_acc (64-127) of that block are
+// accumulated into it. Shared memory holds C and B twice and x three times, so that:
+//   * G of block j+1 is computed while the math warps finish block j-1 and scan block j+1,
 //   * Yoff of block j is computed as soon as the state S_{j-1} is written,
-//   * C, B and x of later blocks are loaded while the current ones are worked on.
+//   * C, B and x of later blocks are loaded while the current ones are worked on; the raw dt of
+//     a block is copied two blocks ahead with cp.async, so no register waits on it.
 // Hand-offs go through mbarriers (tcgen05.commit for the MMAs, TMA transaction counts for
 // the loads, one elected arrival per phase of the math warps); every wait is bounded.
 //
@@ -58,24 +64,25 @@ constexpr int kP = 64;           // head dimension
 constexpr int kN = 128;          // state size
 constexpr int kMath = 256;       // 8 math warps
 constexpr int kThreads = kMath + 32;   // + the control warp
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColG = 0;    // G, two buffers of 128 columns
+constexpr uint32_t kTmemCols = 512;   // 384 used (a power of two is allocated)
+constexpr uint32_t kColG = 0;    // G, two buffers of 128 columns; once masked, a buffer holds
+                                 // Y (columns 0-63) and the state product (64-127) of its block
 constexpr uint32_t kColM = 256;  // M in bf16 pairs (64 columns)
-constexpr uint32_t kColY = 320;
-constexpr uint32_t kColYoff = 384;
-constexpr uint32_t kColS = 448;  // the state product
+constexpr uint32_t kColYoff = 320;
 
 constexpr int kAtom = 16384;     // 128 rows x 128 bytes
 constexpr int kSmC = 0;                       // C, 2 stages x 2 atoms
 constexpr int kSmB = kSmC + 4 * kAtom;        // B, 2 stages x 2 atoms
 constexpr int kSmXw = kSmB + 4 * kAtom;       // w o x, 1 atom
-constexpr int kSmX = kSmXw + kAtom;           // x (then y), 2 stages
-constexpr int kSmS = kSmX + 2 * kAtom;        // bf16 state
-constexpr int kSmArr = kSmS + kAtom;          // per block (2 buffers): cs, dt, e, w, v, each float[kQ]
+constexpr int kSmX = kSmXw + kAtom;           // x (then y), 3 stages
+constexpr int kSmS = kSmX + 3 * kAtom;        // bf16 state
+constexpr int kSmDl = kSmS + kAtom;           // raw delta words, 2 buffers x kQ x 4 bytes
+constexpr int kSmArr = kSmDl + 2 * kQ * 4;    // per block (2 buffers): cs, dt, e, w, v, each float[kQ]
 constexpr int kNArr = 5;
 constexpr int kSmRed = kSmArr + 2 * kNArr * kQ * 4;   // float[8]
-constexpr int kSmBar = kSmRed + 64;           // 10 mbarriers
-constexpr int kSmTmem = kSmBar + 10 * 8;
+constexpr int kNumBars = 11;
+constexpr int kSmBar = kSmRed + 64;           // kNumBars mbarriers
+constexpr int kSmTmem = kSmBar + kNumBars * 8;
 constexpr int kSmFlag = kSmTmem + 8;
 constexpr int kSmemUsed = kSmFlag + 8;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024 bytes
@@ -141,6 +148,16 @@ __device__ __forceinline__ uint4 scale_bf16x8(uint4 v, f2 s2) {
     return r;
 }
 
+// 4-byte asynchronous global -> shared copy (no register is tied up while it is in flight).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ uint4 pack8(const float* v) {
     uint4 r;
     r.x = tc::pack_bf16(v[0], v[1]);
@@ -159,12 +176,12 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
     float* red = reinterpret_cast<float*>(sm + kSmRed);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSmBar);
     uint64_t* full_cb = bars + 0;      // [2] C and B of a stage loaded
-    uint64_t* full_x = bars + 2;       // [2] x of a stage loaded
-    uint64_t* g_done = bars + 4;       // [2] G of a buffer computed
-    uint64_t* yoff_done = bars + 6;    // Yoff of the block computed (all earlier MMAs too)
-    uint64_t* mma2_done = bars + 7;    // Y and the state product computed
-    uint64_t* math_ready = bars + 8;   // M and w o X of the block written
-    uint64_t* epi_done = bars + 9;     // state and y of the block written, accumulators read
+    uint64_t* full_x = bars + 2;       // [3] x of a stage loaded
+    uint64_t* g_done = bars + 5;       // [2] G of a buffer computed
+    uint64_t* yoff_done = bars + 7;    // Yoff of the block computed (all earlier MMAs too)
+    uint64_t* mma2_done = bars + 8;    // Y and the state product computed
+    uint64_t* math_ready = bars + 9;   // M and w o X of the block written, G read
+    uint64_t* epi_done = bars + 10;    // state and y of the block written, accumulators read
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + kSmTmem);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kSmFlag);
 
@@ -178,7 +195,7 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
 
     if (warp == 0) tc::tmem_alloc(tslot, kTmemCols);
     if (tid == kMath) {
-        for (int i = 0; i < 10; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tensormap(&mX);
@@ -197,7 +214,7 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
             const uint32_t aS = smem_u32(sm + kSmS), aXw = smem_u32(sm + kSmXw);
             auto aC = [&](int s) { return smem_u32(sm + kSmC + s * 2 * kAtom); };
             auto aB = [&](int s) { return smem_u32(sm + kSmB + s * 2 * kAtom); };
-            auto aX = [&](int s) { return smem_u32(sm + kSmX + s * kAtom); };
+            auto aX = [&](int j) { return smem_u32(sm + kSmX + (j % 3) * kAtom); };
             auto load_cb = [&](int j) {
                 const int s = j & 1;
                 mbar_arrive_expect_tx(&full_cb[s], 4 * kAtom);
@@ -207,7 +224,7 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
                 tma_load_4d(sm + kSmB + s * 2 * kAtom + kAtom, &mB, 64, grp, j * kQ, b, &full_cb[s]);
             };
             auto load_x = [&](int j) {
-                const int s = j & 1;
+                const int s = j % 3;
                 mbar_arrive_expect_tx(&full_x[s], kAtom);
                 tma_load_4d(sm + kSmX + s * kAtom, &mX, 0, h, j * kQ, b, &full_x[s]);
             };
@@ -233,6 +250,7 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
                     load_cb(1);
                     load_x(1);
                 }
+                if (nblk > 2) load_x(2);
                 if (wait(&full_cb[0], 0)) {
                     tc::fence_after_sync();
                     issue_g(0);
@@ -240,14 +258,32 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
             }
             for (int j = 0; j < nblk && ok; ++j) {
                 const int s = j & 1;
+                // Y_j = M_j X_j and S_acc_j = B_j^T (w o X_j), into the columns of G_j, once
+                // the math warps have masked G_j and written M_j and w o X_j
+                if (!wait(math_ready, j & 1) || !wait(&full_x[j % 3], (j / 3) & 1)) break;
+                tc::fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < kQ / 16; ++k)
+                    tc::mma_ts(tmem + kColG + 128 * s, tmem + kColM + 8 * k,
+                               tc::sdesc_sw128(aX(j) + k * 2048, kAtom, 1024), kIdescY, k > 0);
+#pragma unroll
+                for (int k = 0; k < kQ / 16; ++k)
+                    tc::mma_ss(tmem + kColG + 128 * s + 64, tc::sdesc_sw128(aB(s) + k * 2048, kAtom, 1024),
+                               tc::sdesc_sw128(aXw + k * 2048, kAtom, 1024), kIdescS, k > 0);
+                tc::commit(mma2_done);
                 // the state S_{j-1} is written and the accumulators of block j-1 are read
                 if (!wait(epi_done, j & 1)) break;
                 tc::fence_after_sync();
                 if (j > 0) {
-                    // y of block j-1 (staged in its x buffer) leaves; that buffer takes x_{j+1}
-                    // once the store has read it (below, after this block's products are issued)
-                    tma_store_4d(&mY, 0, h, (j - 1) * kQ, b, sm + kSmX + (s ^ 1) * kAtom);
+                    // y of block j-1 (staged in its x buffer) leaves
+                    tma_store_4d(&mY, 0, h, (j - 1) * kQ, b, sm + kSmX + ((j - 1) % 3) * kAtom);
                     tma_store_commit();
+                }
+                // G_{j+1} into the buffer block j-1's accumulators have left
+                if (j + 1 < nblk) {
+                    if (!wait(&full_cb[s ^ 1], ((j + 1) >> 1) & 1)) break;
+                    tc::fence_after_sync();
+                    issue_g(j + 1);
                 }
                 // Yoff_j = C_j S_{j-1}
 #pragma unroll
@@ -257,40 +293,21 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
                                tc::sdesc_sw128(aS + k * 2048, kAtom, 1024), kIdescYoff, k > 0);
                 }
                 tc::commit(yoff_done);
-                // G_{j+1} into the other buffer (its previous contents, G_{j-1}, were masked
-                // before block j-1's products were issued)
-                if (j + 1 < nblk) {
-                    if (!wait(&full_cb[s ^ 1], ((j + 1) >> 1) & 1)) break;
-                    tc::fence_after_sync();
-                    issue_g(j + 1);
+                // x_{j+2} takes the buffer of y_{j-1} once the store has read it
+                if (j > 0 && j + 2 < nblk) {
+                    tma_store_wait_read<0>();
+                    load_x(j + 2);
                 }
-                // Y_j = M_j X_j and S_acc_j = B_j^T (w o X_j) once M_j and w o X_j are written
-                if (!wait(math_ready, j & 1) || !wait(&full_x[s], (j >> 1) & 1)) break;
-                tc::fence_after_sync();
-#pragma unroll
-                for (int k = 0; k < kQ / 16; ++k)
-                    tc::mma_ts(tmem + kColY, tmem + kColM + 8 * k, tc::sdesc_sw128(aX(s) + k * 2048, kAtom, 1024),
-                               kIdescY, k > 0);
-#pragma unroll
-                for (int k = 0; k < kQ / 16; ++k)
-                    tc::mma_ss(tmem + kColS, tc::sdesc_sw128(aB(s) + k * 2048, kAtom, 1024),
-                               tc::sdesc_sw128(aXw + k * 2048, kAtom, 1024), kIdescS, k > 0);
-                tc::commit(mma2_done);
-                if (j > 0 && j + 1 < nblk) {
-                    tma_store_wait_read<0>();   // y of block j-1 has left x buffer s ^ 1
-                    load_x(j + 1);
-                }
-                // C_j and B_j are free once the products of block j are done: stage s takes
-                // block j+2
+                // C_j and B_j are free once Yoff_j (and everything before it) is done
                 if (j + 2 < nblk) {
-                    if (!wait(mma2_done, j & 1)) break;
+                    if (!wait(yoff_done, j & 1)) break;
                     load_cb(j + 2);
                 }
             }
             if (ok && nblk > 0) {
                 // the last y
                 if (wait(epi_done, nblk & 1)) {
-                    tma_store_4d(&mY, 0, h, (nblk - 1) * kQ, b, sm + kSmX + ((nblk - 1) & 1) * kAtom);
+                    tma_store_4d(&mY, 0, h, (nblk - 1) * kQ, b, sm + kSmX + ((nblk - 1) % 3) * kAtom);
                     tma_store_commit();
                 }
             }
@@ -322,9 +339,23 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
             if (tid == 0) mbar_arrive(bar);
             return !bad;
         };
-        auto load_delta = [&](int j) -> float {
+        // raw delta of block j, row `row`: the aligned 4-byte word holding it is copied into
+        // shared memory (buffer j & 1) without tying up a register; one commit group per block
+        const uintptr_t dl_hi = 2;
+        auto load_delta = [&](int j) {
             const int64_t tt = (int64_t)j * kQ + row;
-            return (half == 0 && j < nblk && tt < L) ? __bfloat162float(delta[((int64_t)b * L + tt) * H + h]) : 0.f;
+            if (half == 0 && j < nblk && tt < L) {
+                const uintptr_t a = reinterpret_cast<uintptr_t>(delta + ((int64_t)b * L + tt) * H + h);
+                cp_async4(sm + kSmDl + (j & 1) * kQ * 4 + row * 4, reinterpret_cast<const void*>(a & ~(uintptr_t)3));
+            }
+            cp_async_commit();
+        };
+        auto read_delta = [&](int j) -> float {
+            const int64_t tt = (int64_t)j * kQ + row;
+            if (half != 0 || tt >= L) return 0.f;
+            const uintptr_t a = reinterpret_cast<uintptr_t>(delta + ((int64_t)b * L + tt) * H + h);
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(sm + kSmDl + (j & 1) * kQ * 4 + row * 4);
+            return (a & dl_hi) ? bf_hi(w) : bf_lo(w);
         };
         // the block scan of dt A_h for block j into array buffer j & 1 (first warpgroup)
         auto scan_block = [&](int j, float draw) {
@@ -381,19 +412,101 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
             for (int c = 0; c < 4; ++c)
                 *reinterpret_cast<uint4*>(sm + kSmS + sw128(row, 4 * half + c)) = pack8(S + 8 * c);
         }
-        scan_block(0, load_delta(0));
+        load_delta(0);
+        load_delta(1);
+        cp_async_wait<1>();
+        scan_block(0, read_delta(0));
         fence_proxy_async_smem();
         bool ok = signal(epi_done, true);    // the initial state is in place
+
+        // epilogue of block jj: y rows into x buffer jj % 3, the state row. Inside the loop the
+        // products of block jj were waited for at the top of block jj + 1 (by then those of
+        // jj + 1 may be done as well, and a second parity wait would take their phase for it)
+        auto epilogue = [&](int jj, bool wait_mma2) -> bool {
+            const int sj = jj & 1;
+            bool okw = !wait_mma2 || wait_warp(mma2_done, jj & 1);
+            okw = okw && wait_warp(yoff_done, jj & 1);
+            tc::fence_after_sync();
+            if (okw) {
+                const int64_t t = (int64_t)jj * kQ + row;
+                const float e_t = arr(sj, 2)[row];
+                const float e_last = red[4 + sj];
+                const __nv_bfloat16* xrow = p.D && t < L ? static_cast<const __nv_bfloat16*>(p.x) +
+                                                               (((int64_t)b * L + t) * H + h) * kP + 32 * half
+                                                         : nullptr;
+                const __nv_bfloat16* zrow = p.z && t < L ? static_cast<const __nv_bfloat16*>(p.z) +
+                                                               (((int64_t)b * L + t) * H + h) * kP + 32 * half
+                                                         : nullptr;
+                unsigned char* ys = sm + kSmX + (jj % 3) * kAtom;
+                const uint32_t colY = kColG + 128 * sj;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t ry[16], ro[16];
+                    tc::ld16(lane_base + colY + 32 * half + 16 * q, ry);
+                    tc::ld16(lane_base + kColYoff + 32 * half + 16 * q, ro);
+                    tc::wait_ld();
+                    float yv[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) yv[i] = fmaf(e_t, __uint_as_float(ro[i]), __uint_as_float(ry[i]));
+                    if (xrow) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 8) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(xrow + 16 * q + i);
+                            yv[i] = fmaf(Dh, bf_lo(v.x), yv[i]);
+                            yv[i + 1] = fmaf(Dh, bf_hi(v.x), yv[i + 1]);
+                            yv[i + 2] = fmaf(Dh, bf_lo(v.y), yv[i + 2]);
+                            yv[i + 3] = fmaf(Dh, bf_hi(v.y), yv[i + 3]);
+                            yv[i + 4] = fmaf(Dh, bf_lo(v.z), yv[i + 4]);
+                            yv[i + 5] = fmaf(Dh, bf_hi(v.z), yv[i + 5]);
+                            yv[i + 6] = fmaf(Dh, bf_lo(v.w), yv[i + 6]);
+                            yv[i + 7] = fmaf(Dh, bf_hi(v.w), yv[i + 7]);
+                        }
+                    }
+                    if (zrow) {
+#pragma unroll
+                        for (int i = 0; i < 16; i += 8) {
+                            const uint4 v = *reinterpret_cast<const uint4*>(zrow + 16 * q + i);
+                            yv[i] *= silu_accurate(bf_lo(v.x));
+                            yv[i + 1] *= silu_accurate(bf_hi(v.x));
+                            yv[i + 2] *= silu_accurate(bf_lo(v.y));
+                            yv[i + 3] *= silu_accurate(bf_hi(v.y));
+                            yv[i + 4] *= silu_accurate(bf_lo(v.z));
+                            yv[i + 5] *= silu_accurate(bf_hi(v.z));
+                            yv[i + 6] *= silu_accurate(bf_lo(v.w));
+                            yv[i + 7] *= silu_accurate(bf_hi(v.w));
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        *reinterpret_cast<uint4*>(ys + sw128(row, 4 * half + 2 * q + c)) = pack8(yv + 8 * c);
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t rs[16];
+                    tc::ld16(lane_base + colY + 64 + 32 * half + 16 * q, rs);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) S[16 * q + i] = fmaf(e_last, S[16 * q + i], __uint_as_float(rs[i]));
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        *reinterpret_cast<uint4*>(sm + kSmS + sw128(row, 4 * half + 2 * q + c)) =
+                            pack8(S + 16 * q + 8 * c);
+                }
+            }
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            return signal(epi_done, okw);
+        };
 
         for (int j = 0; j < nblk && ok; ++j) {
             const int s = j & 1;
             const float* cs = arr(s, 0);
             const float* dts = arr(s, 1);
             const float* vs = arr(s, 4);
-            // delta of block j+1: issued here, used after the mask (no barrier in between)
-            const float draw_next = load_delta(j + 1);
+            // delta of block j+2 (block j's buffer: its scan is done)
+            load_delta(j + 2);
             // ---- wait for x_j and G_j, and for block j-1's products to have consumed M and w o X
-            bool okw = wait_warp(&full_x[s], (j >> 1) & 1) && wait_warp(&g_done[s], (j >> 1) & 1);
+            bool okw = wait_warp(&full_x[j % 3], (j / 3) & 1) && wait_warp(&g_done[s], (j >> 1) & 1);
             if (okw && j > 0) okw = wait_warp(mma2_done, (j - 1) & 1);
             tc::fence_after_sync();
             if (okw) {
@@ -452,7 +565,7 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
                     const int xr = tid >> 1, xg = tid & 1;
                     const float wt = arr(s, 3)[xr];
                     const f2 w2 = pk(wt, wt);
-                    const unsigned char* src = sm + kSmX + s * kAtom + xr * 128;
+                    const unsigned char* src = sm + kSmX + (j % 3) * kAtom + xr * 128;
                     unsigned char* dst = sm + kSmXw + xr * 128;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -468,81 +581,18 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
             ok = signal(math_ready, okw);
             if (!ok) break;
 
-            // ---- the scan of the next block while the tensor core works
-            if (j + 1 < nblk) scan_block(j + 1, draw_next);
-
-            // ---- epilogue: y row t (columns [32 half, +32)) into x buffer s, the state row
-            okw = wait_warp(mma2_done, j & 1) && wait_warp(yoff_done, j & 1);
-            tc::fence_after_sync();
-            if (okw) {
-                const int64_t t = (int64_t)j * kQ + row;
-                const float e_t = arr(s, 2)[row];
-                const float e_last = red[4 + s];
-                const __nv_bfloat16* xrow = p.D && t < L ? static_cast<const __nv_bfloat16*>(p.x) +
-                                                               (((int64_t)b * L + t) * H + h) * kP + 32 * half
-                                                         : nullptr;
-                const __nv_bfloat16* zrow = p.z && t < L ? static_cast<const __nv_bfloat16*>(p.z) +
-                                                               (((int64_t)b * L + t) * H + h) * kP + 32 * half
-                                                         : nullptr;
-                unsigned char* ys = sm + kSmX + s * kAtom;
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    uint32_t ry[16], ro[16];
-                    tc::ld16(lane_base + kColY + 32 * half + 16 * q, ry);
-                    tc::ld16(lane_base + kColYoff + 32 * half + 16 * q, ro);
-                    tc::wait_ld();
-                    float yv[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) yv[i] = fmaf(e_t, __uint_as_float(ro[i]), __uint_as_float(ry[i]));
-                    if (xrow) {
-#pragma unroll
-                        for (int i = 0; i < 16; i += 8) {
-                            const uint4 v = *reinterpret_cast<const uint4*>(xrow + 16 * q + i);
-                            yv[i] = fmaf(Dh, bf_lo(v.x), yv[i]);
-                            yv[i + 1] = fmaf(Dh, bf_hi(v.x), yv[i + 1]);
-                            yv[i + 2] = fmaf(Dh, bf_lo(v.y), yv[i + 2]);
-                            yv[i + 3] = fmaf(Dh, bf_hi(v.y), yv[i + 3]);
-                            yv[i + 4] = fmaf(Dh, bf_lo(v.z), yv[i + 4]);
-                            yv[i + 5] = fmaf(Dh, bf_hi(v.z), yv[i + 5]);
-                            yv[i + 6] = fmaf(Dh, bf_lo(v.w), yv[i + 6]);
-                            yv[i + 7] = fmaf(Dh, bf_hi(v.w), yv[i + 7]);
-                        }
-                    }
-                    if (zrow) {
-#pragma unroll
-                        for (int i = 0; i < 16; i += 8) {
-                            const uint4 v = *reinterpret_cast<const uint4*>(zrow + 16 * q + i);
-                            yv[i] *= silu_accurate(bf_lo(v.x));
-                            yv[i + 1] *= silu_accurate(bf_hi(v.x));
-                            yv[i + 2] *= silu_accurate(bf_lo(v.y));
-                            yv[i + 3] *= silu_accurate(bf_hi(v.y));
-                            yv[i + 4] *= silu_accurate(bf_lo(v.z));
-                            yv[i + 5] *= silu_accurate(bf_hi(v.z));
-                            yv[i + 6] *= silu_accurate(bf_lo(v.w));
-                            yv[i + 7] *= silu_accurate(bf_hi(v.w));
-                        }
-                    }
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-                        *reinterpret_cast<uint4*>(ys + sw128(row, 4 * half + 2 * q + c)) = pack8(yv + 8 * c);
-                }
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    uint32_t rs[16];
-                    tc::ld16(lane_base + kColS + 32 * half + 16 * q, rs);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) S[16 * q + i] = fmaf(e_last, S[16 * q + i], __uint_as_float(rs[i]));
-#pragma unroll
-                    for (int c = 0; c < 2; ++c)
-                        *reinterpret_cast<uint4*>(sm + kSmS + sw128(row, 4 * half + 2 * q + c)) =
-                            pack8(S + 16 * q + 8 * c);
-                }
+            // ---- the epilogue of the previous block while the tensor core works on this one
+            if (j > 0) {
+                ok = epilogue(j - 1, false);
+                if (!ok) break;
             }
-            fence_proxy_async_smem();
-            tc::fence_before_sync();
-            ok = signal(epi_done, okw);
+
+            // ---- the scan of the next block
+            cp_async_wait<1>();
+            if (j + 1 < nblk) scan_block(j + 1, read_delta(j + 1));
         }
+        if (ok && nblk > 0) ok = epilogue(nblk - 1, true);
+        cp_async_wait<0>();   // no copy may land after the block has left
         if (ok && p.h_last) {
             float* dst = p.h_last + (((int64_t)b * H + h) * kN + row) * kP + 32 * half;
 #pragma unroll
