@@ -17,6 +17,12 @@ ssm_scan_ref     Mamba selective scan: softplus(delta + bias), A_bar = exp(delta
 ssd_scan_ref     Mamba-2 recurrence with a scalar A per head, sequential.
                  Pages: "Mamba-2 / SSD" (abeam) "基本アイデア"; "Mamba/SSM complete
                  guide" section 6 "SSD演算の概念".
+causal_conv1d_ref  Causal depthwise conv1d over time (kernel K, left zero padding or the
+                 K-1 previous inputs), then SiLU: the prologue of the Mamba block's x branch.
+                 Pages: "Mamba/SSM complete guide" section 5 `MambaBlock` (nn.Conv1d with
+                 groups = d_inner, kernel d_conv, padding d_conv - 1, output cut to the first
+                 L steps, then F.silu); "論文解説: Mamba" "Mambaブロックの全体構成"
+                 (convolution with d_conv = 4, then SiLU).
 ssd_chunked_ref  The same SSD output through the chunked block decomposition (diagonal
                  blocks by matrix products, chunk-to-chunk hand-off through the state).
                  Pages: "Mamba-2 / SSD" (abeam) "基本アイデア" (diagonal blocks as ordinary
@@ -137,6 +143,38 @@ def softplus(v):
     """log(1 + e^v) in float64, as max(v, 0) + log1p(e^-|v|)."""
     v = np.asarray(v, dtype=np.float64)
     return np.maximum(v, 0.0) + np.log1p(np.exp(-np.abs(v)))
+
+
+def silu(v):
+    """v * sigmoid(v) = v / (1 + e^-v) in float64 (written to avoid overflow of e^-v)."""
+    v = np.asarray(v, dtype=np.float64)
+    e = np.exp(-np.abs(v))
+    return np.where(v >= 0, v / (1.0 + e), v * e / (1.0 + e))
+
+
+def causal_conv1d_ref(x, weight, bias=None, apply_silu=True, x_prev=None):
+    """fp64 causal depthwise convolution along t, then SiLU.
+
+    x (b, L, d); weight (d, K); bias (d) or None; x_prev (b, K-1, d): the K-1 inputs that
+    precede x[:, 0] (zeros when None, which is the zero padding of d_conv - 1 steps on the
+    left). With xp = x_prev followed by x along t,
+        y[b, t, d] = bias[d] + sum_{k=0}^{K-1} weight[d, k] * xp[b, t + k, d],
+    so weight[:, K-1] multiplies x_t and weight[:, 0] multiplies x_{t-K+1} (a convolution
+    layer's cross-correlation, kept to the first L outputs). Then y = silu(y) if apply_silu.
+    Returns y (b, L, d) as float64."""
+    x, weight, bias, x_prev = f64(x), f64(weight), f64(bias), f64(x_prev)
+    b, L, d = x.shape
+    K = weight.shape[1]
+    assert weight.shape == (d, K) and K >= 1
+    assert bias is None or bias.shape == (d,)
+    if x_prev is None:
+        x_prev = np.zeros((b, K - 1, d))
+    assert x_prev.shape == (b, K - 1, d)
+    xp = np.concatenate([x_prev, x], axis=1)          # (b, K - 1 + L, d)
+    y = np.zeros((b, L, d)) if bias is None else np.broadcast_to(bias, (b, L, d)).copy()
+    for k in range(K):
+        y += weight[:, k] * xp[:, k:k + L, :]
+    return silu(y) if apply_silu else y
 
 
 def ssd_chunked_ref(x, delta, A, B, C, chunk, D=None, z=None, delta_bias=None,

@@ -392,3 +392,84 @@ def test_a_planted_index_slip_is_caught(monkeypatch):
     y_bad, _ = oracle.ssm_scan_ref(**bad)
     y_bf, _ = _brute_force_mamba1(p)
     assert np.max(np.abs(y_bad - y_bf)) > 1e-3
+
+
+# ---------------------------------------------------------------- causal conv1d + SiLU prologue
+
+def _conv_problem(rng, b, L, d, K, with_prev=False):
+    x = rng.standard_normal((b, L, d))
+    w = rng.standard_normal((d, K))
+    bias = rng.standard_normal(d)
+    prev = rng.standard_normal((b, K - 1, d)) if with_prev else None
+    return x, w, bias, prev
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 4])
+def test_conv1d_matches_the_pages_layer(K):
+    """The pages' layer is a depthwise convolution with kernel d_conv, padding d_conv - 1 and
+    the output cut to the first L steps, then SiLU: run exactly that through torch's conv1d
+    (float64, CPU) and its SiLU."""
+    import torch
+    rng = _rng(70 + K)
+    b, L, d = 2, 37, 5
+    x, w, bias, _ = _conv_problem(rng, b, L, d, K)
+    xt = torch.from_numpy(x).transpose(1, 2)                            # (b, d, L)
+    ref = torch.nn.functional.conv1d(xt, torch.from_numpy(w)[:, None, :], torch.from_numpy(bias),
+                                     padding=K - 1, groups=d)[:, :, :L]
+    ref = torch.nn.functional.silu(ref).transpose(1, 2).numpy()
+    np.testing.assert_allclose(oracle.causal_conv1d_ref(x, w, bias), ref, rtol=1e-13, atol=1e-13)
+
+
+def test_conv1d_matches_numpy_convolve_per_channel():
+    """Without SiLU each channel is numpy's full convolution with the reversed taps, cut to
+    the first L outputs (causal: output t sees inputs t-K+1 .. t)."""
+    rng = _rng(75)
+    b, L, d, K = 2, 50, 3, 4
+    x, w, bias, _ = _conv_problem(rng, b, L, d, K)
+    y = oracle.causal_conv1d_ref(x, w, bias, apply_silu=False)
+    for bi in range(b):
+        for di in range(d):
+            ref = np.convolve(x[bi, :, di], w[di, ::-1])[:L] + bias[di]
+            np.testing.assert_allclose(y[bi, :, di], ref, rtol=1e-13, atol=1e-13)
+
+
+def test_conv1d_identity_and_delay_taps():
+    """Taps (0, 0, 0, 1) pass x through unchanged; taps (1, 0, 0, 0) delay it by three steps
+    with zeros in front (the causal zero padding)."""
+    rng = _rng(76)
+    x = rng.standard_normal((1, 20, 2))
+    ident = np.tile(np.array([0.0, 0.0, 0.0, 1.0]), (2, 1))
+    np.testing.assert_array_equal(oracle.causal_conv1d_ref(x, ident, apply_silu=False), x)
+    delay = np.tile(np.array([1.0, 0.0, 0.0, 0.0]), (2, 1))
+    y = oracle.causal_conv1d_ref(x, delay, apply_silu=False)
+    np.testing.assert_array_equal(y[:, :3], 0.0)
+    np.testing.assert_array_equal(y[:, 3:], x[:, :-3])
+
+
+def test_conv1d_previous_inputs_resume_a_split_sequence():
+    """Convolving the second half with the last K-1 inputs of the first half as x_prev gives
+    the second half of the convolution of the whole sequence."""
+    rng = _rng(77)
+    b, L, d, K = 2, 40, 3, 4
+    x, w, bias, _ = _conv_problem(rng, b, L, d, K)
+    whole = oracle.causal_conv1d_ref(x, w, bias)
+    first = oracle.causal_conv1d_ref(x[:, :17], w, bias)
+    second = oracle.causal_conv1d_ref(x[:, 17:], w, bias, x_prev=x[:, 17 - (K - 1):17])
+    np.testing.assert_allclose(np.concatenate([first, second], axis=1), whole, rtol=0, atol=1e-14)
+
+
+def test_silu_matches_the_logistic_function():
+    """silu(v) = v * sigmoid(v) against scipy's logistic function, including large |v|."""
+    from scipy.special import expit
+    v = np.array([-800.0, -40.0, -3.5, -1e-8, 0.0, 1e-8, 0.7, 12.0, 800.0])
+    np.testing.assert_allclose(oracle.silu(v), v * expit(v), rtol=1e-15, atol=0)
+
+
+def test_a_planted_conv_tap_reversal_is_caught():
+    """A convolution with its taps in the wrong order (x_t times weight[:, 0]) fails the
+    numpy-convolve pin."""
+    rng = _rng(78)
+    x, w, bias, _ = _conv_problem(rng, 1, 30, 2, 4)
+    bad = oracle.causal_conv1d_ref(x, w[:, ::-1], bias, apply_silu=False)
+    ref = np.convolve(x[0, :, 0], w[0, ::-1])[:30] + bias[0]
+    assert np.max(np.abs(bad[0, :, 0] - ref)) > 1e-3
