@@ -30,7 +30,7 @@
 extern "C" {
 #endif
 
-#define SSMSCAN_ABI_VERSION 1
+#define SSMSCAN_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define SSMSCAN_API __attribute__((visibility("default")))
@@ -80,6 +80,11 @@ typedef enum { SSM_DISC_DELTA_B = 0, SSM_DISC_ZOH = 1 } ssm_discretization_t;
  * Pages: "Mamba/SSM complete guide" section 5, listing `selective_scan` (discretise, loop,
  * readout, u*D) and MambaBlock.forward (y * silu(z)); "論文解説: Mamba" "選択機構"
  * (softplus) and "Hardware-Aware Parallel Scan" (the recurrence, zero initial state).
+ *
+ * Optional prologue (conv_weight != NULL): x is the raw input of the block's x branch, and
+ * the scan runs on u = silu(causal depthwise conv1d(x)) instead, for the input term and the
+ * D skip alike (see ssm_causal_conv1d_fwd for the convolution). Forward direction only
+ * (reverse with the prologue is SSM_ERR_UNSUPPORTED). The convolved input is not written out.
  */
 typedef struct ssm_scan_params {
     int64_t batch;          /* b >= 1 */
@@ -118,6 +123,12 @@ typedef struct ssm_scan_params {
     size_t workspace_bytes;
     int32_t debug_flags;    /* 0 in normal use; SSM_DEBUG_* test hooks */
     int32_t reserved;       /* must be 0 */
+    const float* conv_weight; /* (D, K) fp32 contiguous, or NULL (no prologue: x enters as is) */
+    const float* conv_bias;   /* (D) fp32 or NULL (zero bias) */
+    const void* conv_x_prev;  /* (b, K-1, D) in io_dtype, contiguous: the K-1 raw inputs before
+                                 x[:, 0] (the tail of the previous segment), or NULL (zeros) */
+    int32_t conv_width;       /* K, 1 <= K <= 4, when conv_weight is set; ignored otherwise */
+    int32_t reserved2;        /* must be 0 */
 } ssm_scan_params;
 
 /* Bytes of device workspace ssm_scan_fwd needs for these params (0 if none). Host only,
@@ -149,6 +160,36 @@ SSMSCAN_API ssm_status_t ssm_scan_fwd(const ssm_scan_params* p, void* stream);
  */
 #define SSM_NOALLOC_SCRATCH_BYTES (16u << 20)
 SSMSCAN_API ssm_status_t ssm_scan_fwd_noalloc(const ssm_scan_params* p, void* stream);
+
+/*
+ * Causal depthwise convolution along t with K taps per channel, then optionally SiLU: the
+ * prologue of the Mamba block's x branch,
+ *   v[b,t,d] = bias[d] + sum_{k=0}^{K-1} weight[d,k] * xp[b, t+k, d],   y = silu(v) or v,
+ * where xp is x preceded by the K-1 inputs x_prev (zeros when NULL): weight[d, K-1] multiplies
+ * x_t and weight[d, 0] multiplies x_{t-K+1}. This is a convolution layer with groups = D,
+ * kernel K and padding K-1 whose output is cut to the first L steps.
+ * Pages: "Mamba/SSM complete guide" section 5 `MambaBlock` (nn.Conv1d(d_inner, d_inner,
+ * d_conv, groups = d_inner, padding = d_conv - 1), output [:, :, :L], then F.silu);
+ * "論文解説: Mamba" "Mambaブロックの全体構成" (a d_conv = 4 convolution, then SiLU).
+ * All tensors dense and contiguous; every pointer 16-byte aligned.
+ */
+typedef struct ssm_conv1d_params {
+    int64_t batch;          /* b >= 1 */
+    int64_t seqlen;         /* L >= 0 (0: nothing is launched) */
+    int64_t dim;            /* D >= 1; D * element size must be a multiple of 16 bytes */
+    int32_t width;          /* K, 1 <= K <= 4 */
+    int32_t io_dtype;       /* ssm_dtype_t of x, x_prev and y */
+    int32_t silu;           /* 1: y = silu(v); 0: y = v */
+    int32_t reserved;       /* must be 0 */
+    const void* x;          /* (b, L, D) */
+    const float* weight;    /* (D, K) fp32 */
+    const float* bias;      /* (D) fp32 or NULL */
+    const void* x_prev;     /* (b, K-1, D) or NULL (zeros) */
+    void* y;                /* (b, L, D); must not overlap x or x_prev */
+} ssm_conv1d_params;
+
+/* Enqueue the convolution on `stream`. Returns SSM_OK once launched. */
+SSMSCAN_API ssm_status_t ssm_causal_conv1d_fwd(const ssm_conv1d_params* p, void* stream);
 
 /*
  * Mamba-2 SSD chunked scan: the same recurrence with one scalar A per head and the state

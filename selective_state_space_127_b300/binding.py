@@ -20,12 +20,12 @@ LIB_PATH = os.path.join(_PKG, "libssmscan.so")
 SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_WORKSPACE = range(6)
 SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
 SSM_DISC_DELTA_B, SSM_DISC_ZOH = 0, 1
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 # Every function the header declares (checked by the CPU test suite).
 EXPORTS = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssd_chunk_scan_workspace_size", "ssd_chunk_scan_fwd",
            "ssm_device_status", "ssm_status_string", "ssm_last_error", "ssm_abi_version",
-           "ssm_kernel_launch_count", "ssm_scan_fwd_noalloc")
+           "ssm_kernel_launch_count", "ssm_scan_fwd_noalloc", "ssm_causal_conv1d_fwd")
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _i64, _i32, _vp, _sz = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
@@ -39,7 +39,15 @@ class ScanParams(ctypes.Structure):
                 ("x_stride", _i64 * 3), ("delta_stride", _i64 * 3), ("z_stride", _i64 * 3),
                 ("y_stride", _i64 * 3), ("B_stride", _i64 * 3), ("C_stride", _i64 * 3),
                 ("chunk_len", _i64), ("workspace", _vp), ("workspace_bytes", _sz),
-                ("debug_flags", _i32), ("reserved", _i32)]
+                ("debug_flags", _i32), ("reserved", _i32),
+                ("conv_weight", _vp), ("conv_bias", _vp), ("conv_x_prev", _vp), ("conv_width", _i32),
+                ("reserved2", _i32)]
+
+
+class Conv1dParams(ctypes.Structure):
+    _fields_ = [("batch", _i64), ("seqlen", _i64), ("dim", _i64), ("width", _i32), ("io_dtype", _i32),
+                ("silu", _i32), ("reserved", _i32), ("x", _vp), ("weight", _vp), ("bias", _vp),
+                ("x_prev", _vp), ("y", _vp)]
 
 SSM_DEBUG_SKIP_FIRST_LOAD = 1
 
@@ -89,6 +97,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.ssm_abi_version.restype = ctypes.c_int
             lib.ssm_scan_fwd_noalloc.argtypes = [ctypes.POINTER(ScanParams), _vp]
             lib.ssm_scan_fwd_noalloc.restype = ctypes.c_int
+            lib.ssm_causal_conv1d_fwd.argtypes = [ctypes.POINTER(Conv1dParams), _vp]
+            lib.ssm_causal_conv1d_fwd.restype = ctypes.c_int
             lib.ssm_kernel_launch_count.argtypes = []
             lib.ssm_kernel_launch_count.restype = ctypes.c_uint64
             if lib.ssm_abi_version() != ABI_VERSION:
@@ -142,7 +152,7 @@ def _stream_handle(stream) -> int:
 
 def _scan_params(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_softplus=True, h0=None,
                  reverse=False, zoh=False, chunk_len=0, out=None, return_last_state=True, h_last=None,
-                 debug_flags=0):
+                 debug_flags=0, conv_weight=None, conv_bias=None, conv_x_prev=None):
     """Check the tensors and fill a ScanParams; returns (params, y, h_last)."""
     if not x.is_cuda:
         raise ValueError("x must be a CUDA tensor (use ssm_scan_fwd_host for host buffers)")
@@ -161,6 +171,14 @@ def _scan_params(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_so
     _f32_contig("D", D, (Dm,), dev)
     _f32_contig("delta_bias", delta_bias, (Dm,), dev)
     _f32_contig("h0", h0, (b, Dm, N), dev)
+    K = 0
+    if conv_weight is not None:
+        K = conv_weight.shape[-1]
+        _f32_contig("conv_weight", conv_weight, (Dm, K), dev)
+        _f32_contig("conv_bias", conv_bias, (Dm,), dev)
+        if conv_x_prev is not None and (conv_x_prev.dtype != x.dtype or tuple(conv_x_prev.shape) != (b, K - 1, Dm)
+                                        or not conv_x_prev.is_contiguous() or conv_x_prev.device != dev):
+            raise ValueError(f"conv_x_prev must be contiguous {x.dtype} of shape {(b, K - 1, Dm)} on {dev}")
     y = out if out is not None else torch.empty((b, L, Dm), device=dev, dtype=x.dtype)
     if y.dtype != x.dtype or tuple(y.shape) != (b, L, Dm) or y.device != dev:
         raise ValueError("out has the wrong dtype, shape or device")
@@ -183,6 +201,9 @@ def _scan_params(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_so
     p.C_stride[:] = _strides3(C)
     p.chunk_len = int(chunk_len)
     p.debug_flags = int(debug_flags)
+    if conv_weight is not None:
+        p.conv_weight, p.conv_bias, p.conv_x_prev = _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_x_prev)
+        p.conv_width = K
     return p, y, hl
 
 
@@ -199,16 +220,19 @@ def scan_workspace_size(x, delta, A, B, C, D=None, z=None, delta_bias=None, **kw
 
 def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_softplus=True, h0=None,
                  reverse=False, zoh=False, chunk_len=0, out=None, return_last_state=True, h_last=None,
-                 stream=None, workspace=None, debug_flags=0):
+                 stream=None, workspace=None, debug_flags=0, conv_weight=None, conv_bias=None, conv_x_prev=None):
     """Selective scan on the GPU. x, delta, z: (b, L, D); B, C: (b, L, N); A: (D, N) fp32;
     D, delta_bias: (D) fp32; h0: (b, D, N) fp32. I/O tensors are fp32 or bf16 (all alike) and
     may be strided (delta's channel stride may be 0). ``workspace`` (a uint8 CUDA tensor of at
     least scan_workspace_size() bytes, 256-byte aligned) is allocated when not given.
-    Returns (y, h_last or None)."""
+    With ``conv_weight`` (D, K) fp32 (K <= 4), x is the raw input and the scan runs on
+    silu(causal conv1d(x) + conv_bias); ``conv_x_prev`` (b, K-1, D) holds the K-1 raw inputs
+    before x[:, 0] (zeros when None). Returns (y, h_last or None)."""
     lib = load_library()
     p, y, hl = _scan_params(x, delta, A, B, C, D, z, delta_bias, delta_softplus=delta_softplus, h0=h0,
                             reverse=reverse, zoh=zoh, chunk_len=chunk_len, out=out,
-                            return_last_state=return_last_state, h_last=h_last, debug_flags=debug_flags)
+                            return_last_state=return_last_state, h_last=h_last, debug_flags=debug_flags,
+                            conv_weight=conv_weight, conv_bias=conv_bias, conv_x_prev=conv_x_prev)
     ws_bytes = lib.ssm_scan_workspace_size(ctypes.byref(p))
     if ws_bytes == ctypes.c_size_t(-1).value:
         _check(lib, lib.ssm_scan_fwd(ctypes.byref(p), None))  # raises with the reason
@@ -233,6 +257,34 @@ def ssm_scan_fwd_noalloc(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, 
     with torch.cuda.device(x.device):
         _check(lib, lib.ssm_scan_fwd_noalloc(ctypes.byref(p), _stream_handle(stream)))
     return y, hl
+
+
+def causal_conv1d_fwd(x, weight, bias=None, *, silu=True, x_prev=None, out=None, stream=None):
+    """Causal depthwise conv1d along t (then SiLU when ``silu``) on the GPU. x: (b, L, D)
+    contiguous fp32 or bf16 with D * element size a multiple of 16 bytes; weight: (D, K) fp32
+    (K <= 4; weight[:, K-1] multiplies x_t); bias: (D) fp32; x_prev: (b, K-1, D) like x, the
+    inputs before x[:, 0] (zeros when None). Returns y (b, L, D) in x's dtype."""
+    lib = load_library()
+    if not x.is_cuda or not x.is_contiguous() or x.dim() != 3:
+        raise ValueError("x must be a contiguous (b, L, D) CUDA tensor")
+    dev = x.device
+    b, L, Dm = x.shape
+    K = weight.shape[-1]
+    _f32_contig("weight", weight, (Dm, K), dev)
+    _f32_contig("bias", bias, (Dm,), dev)
+    if x_prev is not None and (x_prev.dtype != x.dtype or tuple(x_prev.shape) != (b, K - 1, Dm)
+                               or not x_prev.is_contiguous() or x_prev.device != dev):
+        raise ValueError(f"x_prev must be contiguous {x.dtype} of shape {(b, K - 1, Dm)} on {dev}")
+    y = out if out is not None else torch.empty_like(x)
+    if y.dtype != x.dtype or tuple(y.shape) != (b, L, Dm) or not y.is_contiguous() or y.device != dev:
+        raise ValueError("out has the wrong dtype, shape, layout or device")
+    p = Conv1dParams()
+    p.batch, p.seqlen, p.dim, p.width = b, L, Dm, K
+    p.io_dtype, p.silu = _io_dtype(x), int(bool(silu))
+    p.x, p.weight, p.bias, p.x_prev, p.y = _ptr(x), _ptr(weight), _ptr(bias), _ptr(x_prev), _ptr(y)
+    with torch.cuda.device(dev):
+        _check(lib, lib.ssm_causal_conv1d_fwd(ctypes.byref(p), _stream_handle(stream)))
+    return y
 
 
 def ssd_chunk_scan_fwd(x, delta, A, B, C, chunk_size=256, D=None, z=None, delta_bias=None, *,

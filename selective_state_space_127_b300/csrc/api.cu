@@ -68,6 +68,7 @@ bool non_overlapping(const int64_t* sizes, const int64_t* st, int nd) {
 }
 
 constexpr int64_t kMaxDState = 256;
+constexpr int kMaxConvWidth = 4;
 
 ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
     if (!p) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
@@ -84,13 +85,20 @@ ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
     if ((p->delta_softplus != 0 && p->delta_softplus != 1) || (p->reverse != 0 && p->reverse != 1))
         return fail(SSM_ERR_INVALID_ARG, "delta_softplus and reverse must be 0 or 1");
     if (p->chunk_len < 0) return fail(SSM_ERR_INVALID_ARG, "chunk_len must be >= 0");
-    if (p->reserved != 0 || (p->debug_flags & ~SSM_DEBUG_SKIP_FIRST_LOAD) != 0)
+    if (p->reserved != 0 || p->reserved2 != 0 || (p->debug_flags & ~SSM_DEBUG_SKIP_FIRST_LOAD) != 0)
         return fail(SSM_ERR_INVALID_ARG, "unknown debug_flags or nonzero reserved field");
     if (!p->A) return fail(SSM_ERR_INVALID_ARG, "A is NULL");
+    if (p->conv_weight) {
+        if (p->conv_width < 1 || p->conv_width > kMaxConvWidth)
+            return fail(SSM_ERR_INVALID_ARG, "conv_width must be 1..%d (got %d)", kMaxConvWidth, p->conv_width);
+        if (p->reverse) return fail(SSM_ERR_UNSUPPORTED, "the conv1d prologue runs forward only");
+        if (!aligned(p->conv_weight, 4) || (p->conv_bias && !aligned(p->conv_bias, 4)))
+            return fail(SSM_ERR_INVALID_ARG, "conv_weight and conv_bias must be 4-byte aligned");
+    }
     if (p->seqlen > 0 && (!p->x || !p->delta || !p->B || !p->C || !p->y))
         return fail(SSM_ERR_INVALID_ARG, "x, delta, B, C and y are required");
     const size_t esz = p->io_dtype == SSM_DTYPE_BF16 ? 2 : 4;
-    const void* io[] = {p->x, p->delta, p->B, p->C, p->z, p->y};
+    const void* io[] = {p->x, p->delta, p->B, p->C, p->z, p->y, p->conv_weight ? p->conv_x_prev : nullptr};
     for (const void* q : io)
         if (q && !aligned(q, esz)) return fail(SSM_ERR_INVALID_ARG, "I/O pointer not aligned to its dtype");
     const void* f32[] = {p->A, p->D, p->delta_bias, p->h0, p->h_last};
@@ -140,6 +148,55 @@ ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
     a.workspace = p->workspace;
     a.workspace_bytes = p->workspace_bytes;
     a.debug_flags = p->debug_flags;
+    a.conv_w = p->conv_weight;
+    a.conv_b = p->conv_weight ? p->conv_bias : nullptr;
+    a.conv_prev = p->conv_weight ? p->conv_x_prev : nullptr;
+    a.conv_k = p->conv_weight ? p->conv_width : 0;
+    return SSM_OK;
+}
+
+ssm_status_t validate_conv1d(const ssm_conv1d_params* p, ssm::Conv1dArgs* out) {
+    if (!p) return fail(SSM_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1 || p->dim < 1 || p->seqlen < 0)
+        return fail(SSM_ERR_INVALID_ARG, "need batch >= 1, dim >= 1, seqlen >= 0");
+    if (p->width < 1 || p->width > kMaxConvWidth)
+        return fail(SSM_ERR_INVALID_ARG, "width must be 1..%d (got %d)", kMaxConvWidth, p->width);
+    if (p->io_dtype != SSM_DTYPE_F32 && p->io_dtype != SSM_DTYPE_BF16)
+        return fail(SSM_ERR_INVALID_ARG, "io_dtype %d unknown", p->io_dtype);
+    if ((p->silu != 0 && p->silu != 1) || p->reserved != 0)
+        return fail(SSM_ERR_INVALID_ARG, "silu must be 0 or 1 and reserved 0");
+    if (!p->weight) return fail(SSM_ERR_INVALID_ARG, "weight is NULL");
+    if (p->seqlen > 0 && (!p->x || !p->y)) return fail(SSM_ERR_INVALID_ARG, "x and y are required");
+    const size_t esz = p->io_dtype == SSM_DTYPE_BF16 ? 2 : 4;
+    if ((p->dim * (int64_t)esz) % 16 != 0)
+        return fail(SSM_ERR_UNSUPPORTED, "dim * element size must be a multiple of 16 bytes");
+    const void* io[] = {p->x, p->x_prev, p->y};
+    for (const void* q : io)
+        if (q && !aligned(q, 16)) return fail(SSM_ERR_INVALID_ARG, "x, x_prev and y must be 16-byte aligned");
+    if (!aligned(p->weight, 4) || (p->bias && !aligned(p->bias, 4)))
+        return fail(SSM_ERR_INVALID_ARG, "weight and bias must be 4-byte aligned");
+    if (p->seqlen > 0) {
+        const char* y0 = static_cast<const char*>(p->y);
+        const int64_t ybytes = p->batch * p->seqlen * p->dim * (int64_t)esz;
+        auto overlaps = [&](const void* q, int64_t bytes) {
+            const char* q0 = static_cast<const char*>(q);
+            return q && q0 < y0 + ybytes && y0 < q0 + bytes;
+        };
+        if (overlaps(p->x, ybytes) || overlaps(p->x_prev, p->batch * (p->width - 1) * p->dim * (int64_t)esz))
+            return fail(SSM_ERR_INVALID_ARG, "y overlaps x or x_prev");
+    }
+    ssm::Conv1dArgs& a = *out;
+    a.batch = p->batch;
+    a.seqlen = p->seqlen;
+    a.dim = p->dim;
+    a.k = p->width;
+    a.io_bf16 = p->io_dtype == SSM_DTYPE_BF16;
+    a.silu = p->silu;
+    a.x = p->x;
+    a.w = p->weight;
+    a.bias = p->bias;
+    a.x_prev = p->x_prev;
+    a.y = p->y;
     return SSM_OK;
 }
 
@@ -248,6 +305,16 @@ ssm_status_t ssm_scan_fwd(const ssm_scan_params* p, void* stream) {
     } else {
         e = ssm::launch_scan_generic(a, st);
     }
+    if (e != cudaSuccess) return cuda_fail(e);
+    return ok();
+}
+
+ssm_status_t ssm_causal_conv1d_fwd(const ssm_conv1d_params* p, void* stream) {
+    ssm::Conv1dArgs a;
+    ssm_status_t s = validate_conv1d(p, &a);
+    if (s != SSM_OK) return s;
+    if (a.seqlen == 0) return ok();
+    cudaError_t e = ssm::launch_conv1d(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return ok();
 }

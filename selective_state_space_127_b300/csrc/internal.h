@@ -30,6 +30,23 @@ struct ScanArgs {
     void* workspace;
     size_t workspace_bytes;
     int debug_flags;
+    // causal conv1d + SiLU prologue on x (conv_w == nullptr: none)
+    const float* conv_w;     // (D, K)
+    const float* conv_b;     // (D) or nullptr
+    const void* conv_prev;   // (b, K-1, D) io dtype or nullptr
+    int conv_k;
+};
+
+struct Conv1dArgs {
+    int64_t batch, seqlen, dim;
+    int k;
+    int io_bf16;
+    int silu;
+    const void* x;
+    const float* w;
+    const float* bias;
+    const void* x_prev;
+    void* y;
 };
 
 struct SSDArgs {
@@ -66,6 +83,7 @@ unsigned* device_status_ptr();
 cudaError_t read_device_status(unsigned* out, bool clear, cudaStream_t st);
 
 // Kernel launchers: return cudaSuccess or the launch error. They assume valid args.
+cudaError_t launch_conv1d(const Conv1dArgs& a, cudaStream_t st);
 cudaError_t launch_scan_generic(const ScanArgs& a, cudaStream_t s);
 bool scan_fast_supported(const ScanArgs& a);
 // Steps per chunk the fast path uses (a multiple of its tile; >= seqlen when not split) and

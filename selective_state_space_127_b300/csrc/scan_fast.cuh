@@ -1,0 +1,442 @@
+// Kernel template of the fast (TMA) selective scan, shared by the translation unit of the
+// plain kernels (scan_fast.cu) and that of the kernels with the conv1d + SiLU prologue
+// (scan_fast_conv.cu), so the two sets compile in parallel. The design notes are at the top of
+// scan_fast.cu.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tma.cuh"
+
+namespace ssm {
+namespace fast {
+
+
+constexpr int kCh = 16;        // channels per CTA
+constexpr int kT = 32;         // steps per tile
+constexpr int kStages = 3;     // TMA ring depth
+
+enum Mode { kFull = 0, kPass1 = 1 };
+
+struct FastParams {
+    int64_t seqlen;
+    int64_t chunk;         // steps per chunk (multiple of kT); >= seqlen when not split
+    int dim;
+    int nchunks;
+    const float* A;
+    const float* D;
+    const float* bias;
+    const float* h0;
+    float* h_last;
+    float* carry;          // (nchunks - 1, b, D, N): local end states, then initial states
+    float* sumdt;          // (nchunks - 1, b, D)
+    unsigned* status;
+    int skip_first_load;   // test hook: never issue tile 0 (only used when the sequence is one tile)
+    // conv1d + SiLU prologue (CONV kernels only)
+    const float* conv_w;   // (D, conv_k)
+    const float* conv_b;   // (D) or nullptr
+    const void* conv_prev; // (b, conv_k - 1, D) or nullptr
+    int conv_k;
+};
+
+// Rows of x before a tile that the conv prologue reads (the widest kernel, 4 taps, needs 3).
+constexpr int kHalo = 3;
+
+template <int N, bool BF16, bool CONV>
+struct Layout {
+    static constexpr int kEsz = BF16 ? 2 : 4;
+    static constexpr int kTileX = kT * kCh * kEsz;          // one of x, delta, z, y
+    static constexpr int kTileB = kT * N * kEsz;            // one of B, C
+    static constexpr int kXRows = kT + (CONV ? kHalo : 0);  // x rows loaded per tile
+    static constexpr int kXBox = kXRows * kCh * kEsz;       // bytes of the x box
+    static constexpr int kOffD = (kXBox + 127) / 128 * 128; // delta, z, B, C follow x
+    static constexpr int kOffZ = kOffD + kTileX;
+    static constexpr int kOffB = kOffZ + kTileX;
+    static constexpr int kOffC = kOffB + kTileB;
+    static constexpr int kStageBytes = kOffC + kTileB;
+    static constexpr int kStageStride = (kStageBytes + 127) / 128 * 128;
+    static constexpr int kBars = 0;                                   // kStages mbarriers
+    static constexpr int kRing = 128;
+    static constexpr int kBCf = kRing + kStages * kStageStride;       // fp32 B then C [kT][N]
+    static constexpr int kY = kBCf + 2 * kT * N * 4;                  // 2 y tiles
+    static constexpr int kYStride = (kTileX + 127) / 128 * 128;
+    static constexpr int kTotal = kY + 2 * kYStride;
+};
+
+__device__ __forceinline__ float ld_io(const void* base, int i, bool bf16) {
+    return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]) : static_cast<const float*>(base)[i];
+}
+
+// Per-(step, channel) scalars one lane computes for its step of a group.
+struct Scal {
+    float dt, u, dx, gate;
+};
+
+// Conv prologue taps of one channel, right-aligned: w[3] multiplies x_t, w[0] x_{t-3}.
+struct ConvTaps {
+    float w[4];
+    float b;
+};
+
+template <bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS, bool CONV>
+__device__ __forceinline__ Scal scalars(const void* xs, const void* ds, const void* zs, int jj, int c, float bias,
+                                        float Dd, bool tv, const ConvTaps& ct) {
+    Scal r;
+    float xr;
+    if constexpr (CONV) {
+        // the x tile starts kHalo rows early: rows jj .. jj + 3 hold x_{t-3} .. x_t
+        float v = ct.b;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v = fmaf(ct.w[j], ld_io(xs, (jj + j) * kCh + c, BF16), v);
+        xr = silu_fast(v);
+    } else {
+        xr = ld_io(xs, jj * kCh + c, BF16);
+    }
+    float dt = ld_io(ds, jj * kCh + c, BF16) + bias;
+    if constexpr (SOFTPLUS) dt = softplus_fast(dt);
+    r.dt = tv ? dt : 0.f;
+    r.u = r.dt * xr;
+    r.dx = DSKIP ? Dd * xr : 0.f;
+    r.gate = GATE ? silu_fast(ld_io(zs, jj * kCh + c, BF16)) : 1.f;
+    return r;
+}
+
+// S consecutive fp32 values of a shared-memory row as S / 2 packed pairs.
+template <int S>
+__device__ __forceinline__ void lds_pairs(const float* p, f2 (&v)[S / 2]) {
+    if constexpr (S % 4 == 0) {
+#pragma unroll
+        for (int k = 0; k < S / 2; k += 2) {
+            const ulonglong2 q = *reinterpret_cast<const ulonglong2*>(p + 2 * k);
+            v[k] = q.x;
+            v[k + 1] = q.y;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < S / 2; ++k) v[k] = *reinterpret_cast<const unsigned long long*>(p + 2 * k);
+    }
+}
+
+template <int N, bool BF16, int LPC, bool GATE, bool DSKIP, bool SOFTPLUS, int MODE, bool CONV>
+__global__ void __launch_bounds__(kCh * LPC, 16 / LPC)
+scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap md,
+                 const __grid_constant__ CUtensorMap mz, const __grid_constant__ CUtensorMap mB,
+                 const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap my,
+                 const FastParams p) {
+    using Lay = Layout<N, BF16, CONV>;
+    constexpr int kThreads = kCh * LPC;
+    constexpr int S = N / LPC;         // states per lane
+    constexpr int P = S / 2;           // packed pairs per lane
+    constexpr bool kReadout = MODE == kFull;
+    constexpr bool kGate = GATE && kReadout;
+    static_assert(S % 2 == 0, "states per lane must be even");
+    static_assert(LPC == 2 || LPC == 4 || LPC == 8, "2, 4 or 8 lanes per channel");
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBars);
+
+    const int tid = threadIdx.x;
+    const int c = tid / LPC, g = tid % LPC;
+    const int d0 = blockIdx.x * kCh;
+    const int b = blockIdx.y;
+    const int chunk = blockIdx.z;
+    const int d = d0 + c;
+    const bool dvalid = d < p.dim;
+    const int64_t t_begin = (int64_t)chunk * p.chunk;
+    const int64_t t_end = t_begin + p.chunk < p.seqlen ? t_begin + p.chunk : p.seqlen;
+    const int64_t len = t_end - t_begin;
+    const int ntiles = (int)((len + kT - 1) / kT);
+
+    // initial state: h0 for the first chunk, the carried state for the others (pass 2),
+    // zero in pass 1
+    const float* hinit = nullptr;
+    if constexpr (MODE == kFull) {
+        if (chunk == 0)
+            hinit = p.h0 ? p.h0 + ((int64_t)b * p.dim) * N : nullptr;
+        else
+            hinit = p.carry + ((int64_t)(chunk - 1) * gridDim.y + b) * p.dim * N;
+    }
+    f2 A2[P], h[P];
+#pragma unroll
+    for (int k = 0; k < P; ++k) {
+        const int n = g * S + 2 * k;
+        float a0 = 0.f, a1 = 0.f, h0v = 0.f, h1v = 0.f;
+        if (dvalid) {
+            a0 = p.A[(int64_t)d * N + n] * kLog2e;
+            a1 = p.A[(int64_t)d * N + n + 1] * kLog2e;
+            if (hinit) {
+                h0v = hinit[(int64_t)d * N + n];
+                h1v = hinit[(int64_t)d * N + n + 1];
+            }
+        }
+        A2[k] = pk(a0, a1);
+        h[k] = pk(h0v, h1v);
+    }
+    const float bias = (dvalid && p.bias) ? p.bias[d] : 0.f;
+    const float Dd = (DSKIP && dvalid) ? p.D[d] : 0.f;
+    float dtsum = 0.f;   // pass 1: sum of dt over the chunk
+    ConvTaps ct{{0.f, 0.f, 0.f, 0.f}, 0.f};
+    if constexpr (CONV) {
+        if (dvalid) {
+            const int K = p.conv_k;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j >= 4 - K) ct.w[j] = p.conv_w[(int64_t)d * K + j - (4 - K)];
+            ct.b = p.conv_b ? p.conv_b[d] : 0.f;
+        }
+    }
+
+    auto stage_ptr = [&](int buf) { return smem + Lay::kRing + buf * Lay::kStageStride; };
+    auto issue = [&](int s) {
+        const int buf = s % kStages;
+        unsigned char* st = stage_ptr(buf);
+        constexpr unsigned kBytes =
+            Lay::kXBox + Lay::kTileX + (kGate ? Lay::kTileX : 0) + Lay::kTileB + (kReadout ? Lay::kTileB : 0);
+        mbar_arrive_expect_tx(&bars[buf], kBytes);
+        const int t0 = (int)(t_begin + (int64_t)s * kT);
+        // with the conv prologue the x box starts kHalo rows early (zero-filled before t = 0)
+        tma_load_3d(st, &mx, d0, CONV ? t0 - kHalo : t0, b, &bars[buf]);
+        tma_load_3d(st + Lay::kOffD, &md, d0, t0, b, &bars[buf]);
+        if constexpr (kGate) tma_load_3d(st + Lay::kOffZ, &mz, d0, t0, b, &bars[buf]);
+        tma_load_3d(st + Lay::kOffB, &mB, 0, t0, b, &bars[buf]);
+        if constexpr (kReadout) tma_load_3d(st + Lay::kOffC, &mC, 0, t0, b, &bars[buf]);
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        prefetch_tensormap(&mx);
+        prefetch_tensormap(&mB);
+        for (int s = p.skip_first_load ? 1 : 0; s < kStages && s < ntiles; ++s) issue(s);
+    }
+    __syncthreads();
+
+    bool failed = false;
+    for (int s = 0; s < ntiles; ++s) {
+        const int buf = s % kStages;
+        const bool ok = mbar_wait_bounded(&bars[buf], (s / kStages) & 1, p.status);
+        if (__syncthreads_or(!ok)) {
+            // give up on this tile; before leaving, wait (bounded) for the later tiles
+            // already issued so that no copy still targets this CTA's shared memory
+            if (tid == 0)
+                for (int s2 = s + 1; s2 < s + kStages && s2 < ntiles; ++s2)
+                    mbar_wait_bounded(&bars[s2 % kStages], (s2 / kStages) & 1, p.status);
+            failed = true;
+            break;
+        }
+        unsigned char* st = stage_ptr(buf);
+        const void* xs = st;
+        const void* ds = st + Lay::kOffD;
+        const void* zs = st + Lay::kOffZ;
+        if constexpr (CONV) {
+            // the first tile of the sequence: the rows before t = 0 hold the given previous
+            // inputs instead of the zero fill
+            if (chunk == 0 && s == 0 && p.conv_prev) {
+                const int K = p.conv_k;
+                for (int i = tid; i < kHalo * kCh; i += kThreads) {
+                    const int r = i / kCh, cc = i % kCh, m = kHalo - r;   // row r holds x_{-m}
+                    if (m <= K - 1 && d0 + cc < p.dim) {
+                        const int64_t src = ((int64_t)b * (K - 1) + (K - 1 - m)) * p.dim + d0 + cc;
+                        if constexpr (BF16)
+                            reinterpret_cast<__nv_bfloat16*>(st)[i] =
+                                static_cast<const __nv_bfloat16*>(p.conv_prev)[src];
+                        else
+                            reinterpret_cast<float*>(st)[i] = static_cast<const float*>(p.conv_prev)[src];
+                    }
+                }
+                fence_proxy_async_smem();   // this slot is a TMA destination again later
+            }
+        }
+        // B (and C) of the tile widened to fp32
+        float* bcf = reinterpret_cast<float*>(smem + Lay::kBCf);
+        if constexpr (BF16) {
+            const uint4* src = reinterpret_cast<const uint4*>(st + Lay::kOffB);
+            constexpr int kChunks = (kReadout ? 2 : 1) * kT * N / 8;
+#pragma unroll
+            for (int i = tid; i < kChunks; i += kThreads) {
+                const uint4 v = src[i];
+                float4* dst = reinterpret_cast<float4*>(bcf + i * 8);
+                dst[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                                     __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+                dst[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u),
+                                     __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+            }
+        } else {
+            const float4* src = reinterpret_cast<const float4*>(st + Lay::kOffB);
+            constexpr int kChunks = (kReadout ? 2 : 1) * kT * N / 4;
+#pragma unroll
+            for (int i = tid; i < kChunks; i += kThreads) reinterpret_cast<float4*>(bcf)[i] = src[i];
+        }
+        const float* Bf = bcf;
+        const float* Cf = bcf + kT * N;
+        unsigned char* ys = smem + Lay::kY + (s & 1) * Lay::kYStride;
+        if (kReadout && s >= 2 && tid == 0) tma_store_wait_read<1>();   // the store of tile s-2 read ys
+        __syncthreads();
+        const int rem = (int)(len - (int64_t)s * kT);
+        const int tcount = rem < kT ? rem : kT;
+
+        float yout[kT / LPC];   // the steps this lane finishes; stored after the loop so that no
+                                // shared-memory store sits between the loads of later steps
+        Scal cur = scalars<BF16, kGate, DSKIP && kReadout, SOFTPLUS, CONV>(xs, ds, zs, g, c, bias, Dd, g < tcount, ct);
+#pragma unroll
+        for (int grp = 0; grp < kT / LPC; ++grp) {
+            // the next group's scalars: independent of the state, overlaps the updates below
+            const int jn = (grp + 1) * LPC + g;
+            const Scal nxt = scalars<BF16, kGate, DSKIP && kReadout, SOFTPLUS, CONV>(
+                xs, ds, zs, jn < kT ? jn : g, c, bias, Dd, jn < tcount, ct);
+            float acc[LPC];
+#pragma unroll
+            for (int q = 0; q < LPC; ++q) {
+                const float dtq = __shfl_sync(0xffffffffu, cur.dt, q, LPC);
+                const float uq = __shfl_sync(0xffffffffu, cur.u, q, LPC);
+                if constexpr (MODE == kPass1) dtsum += dtq;
+                const f2 dt2 = pk(dtq, dtq), u2 = pk(uq, uq);
+                f2 bv[P];
+                lds_pairs<S>(Bf + (grp * LPC + q) * N + g * S, bv);
+                f2 cv[P];
+                if constexpr (kReadout) lds_pairs<S>(Cf + (grp * LPC + q) * N + g * S, cv);
+                f2 a2 = pk(0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < P; ++k) {
+                    float e0, e1;
+                    upk(mul2(dt2, A2[k]), e0, e1);
+                    const f2 ab = pk(ex2_approx(e0), ex2_approx(e1));
+                    h[k] = fma2(ab, h[k], mul2(u2, bv[k]));
+                    if constexpr (kReadout) a2 = fma2(cv[k], h[k], a2);
+                }
+                if constexpr (kReadout) {
+                    float lo, hi;
+                    upk(a2, lo, hi);
+                    acc[q] = lo + hi;
+                }
+            }
+            if constexpr (kReadout) {
+                // reduce-scatter over the LPC lanes of the channel: each round a lane keeps the
+                // half of its partial sums whose step index has its lane bit and adds the
+                // partner's; lane g ends with the full sum of step g
+#pragma unroll
+                for (int m = LPC / 2; m >= 1; m >>= 1) {
+                    const bool upper = (g & m) != 0;
+#pragma unroll
+                    for (int i = 0; i < m; ++i) {
+                        const float keep = upper ? acc[i + m] : acc[i];
+                        const float send = upper ? acc[i] : acc[i + m];
+                        acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                    }
+                }
+                yout[grp] = (acc[0] + cur.dx) * cur.gate;
+            }
+            cur = nxt;
+        }
+        if constexpr (kReadout) {
+#pragma unroll
+            for (int grp = 0; grp < kT / LPC; ++grp) {
+                const int jj = grp * LPC + g;
+                if constexpr (BF16)
+                    reinterpret_cast<__nv_bfloat16*>(ys)[jj * kCh + c] = __float2bfloat16_rn(yout[grp]);
+                else
+                    reinterpret_cast<float*>(ys)[jj * kCh + c] = yout[grp];
+            }
+            fence_proxy_async_smem();
+        }
+        __syncthreads();
+        if (tid == 0) {
+            if constexpr (kReadout) {
+                tma_store_3d(&my, d0, (int)(t_begin + (int64_t)s * kT), b, ys);
+                tma_store_commit();
+            }
+            if (s + kStages < ntiles) issue(s + kStages);
+        }
+    }
+    if (kReadout && tid == 0) tma_store_wait_all();
+    if (failed) return;
+    if (!dvalid) return;
+    if constexpr (MODE == kFull) {
+        if (p.h_last && chunk == (int)gridDim.z - 1) {
+            float* out = p.h_last + ((int64_t)b * p.dim + d) * N;
+#pragma unroll
+            for (int k = 0; k < P; ++k) {
+                float lo, hi;
+                upk(h[k], lo, hi);
+                *reinterpret_cast<float2*>(out + g * S + 2 * k) = make_float2(lo, hi);
+            }
+        }
+    } else {
+        float* out = p.carry + (((int64_t)chunk * gridDim.y + b) * p.dim + d) * N;
+#pragma unroll
+        for (int k = 0; k < P; ++k) {
+            float lo, hi;
+            upk(h[k], lo, hi);
+            *reinterpret_cast<float2*>(out + g * S + 2 * k) = make_float2(lo, hi);
+        }
+        if (g == 0) p.sumdt[((int64_t)chunk * gridDim.y + b) * p.dim + d] = dtsum;
+    }
+}
+
+// Lanes per channel: N / 8, so every lane keeps 8 states (4 packed pairs). Measured on the
+// b8 D1536 L2048 N16 bf16 workload: 2 lanes 177 us, 4 lanes 194 us, 8 lanes 236 us -- eight
+// independent state chains per lane hide the SFU and shared-memory latency better than more
+// warps with fewer states each.
+template <int N>
+constexpr int lanes_per_channel() { return N / 8; }
+
+template <int N, bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS, int MODE, bool CONV,
+          int LPC = lanes_per_channel<N>()>
+cudaError_t launch_t(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz, cudaStream_t st) {
+    using Lay = Layout<N, BF16, CONV>;
+    auto kern = scan_fast_kernel<N, BF16, LPC, GATE, DSKIP, SOFTPLUS, MODE, CONV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kTotal);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)((a.dim + kCh - 1) / kCh), (unsigned)a.batch, (unsigned)nz);
+    kern<<<grid, kCh * LPC, Lay::kTotal, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], fp);
+    note_launches(1);
+    return cudaGetLastError();
+}
+
+template <int N, bool BF16, int MODE, bool CONV>
+cudaError_t dispatch_flags(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz, cudaStream_t st) {
+    const bool gate = a.z != nullptr, dskip = a.D != nullptr, sp = a.softplus != 0;
+    if constexpr (MODE == kPass1) {
+        // pass 1 reads neither z nor D
+        return sp ? launch_t<N, BF16, false, false, true, MODE, CONV>(maps, fp, a, nz, st)
+                  : launch_t<N, BF16, false, false, false, MODE, CONV>(maps, fp, a, nz, st);
+    } else {
+#define SSM_FAST_CASE(G_, D_, S_) \
+    if (gate == G_ && dskip == D_ && sp == S_) return launch_t<N, BF16, G_, D_, S_, MODE, CONV>(maps, fp, a, nz, st);
+        SSM_FAST_CASE(true, true, true)
+        SSM_FAST_CASE(true, true, false)
+        SSM_FAST_CASE(true, false, true)
+        SSM_FAST_CASE(true, false, false)
+        SSM_FAST_CASE(false, true, true)
+        SSM_FAST_CASE(false, true, false)
+        SSM_FAST_CASE(false, false, true)
+        SSM_FAST_CASE(false, false, false)
+#undef SSM_FAST_CASE
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <int MODE, bool CONV>
+cudaError_t dispatch(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz, cudaStream_t st) {
+    const bool bf = a.io_bf16 != 0;
+    switch (a.dstate) {
+        case 16: return bf ? dispatch_flags<16, true, MODE, CONV>(maps, fp, a, nz, st)
+                           : dispatch_flags<16, false, MODE, CONV>(maps, fp, a, nz, st);
+        case 32: return bf ? dispatch_flags<32, true, MODE, CONV>(maps, fp, a, nz, st)
+                           : dispatch_flags<32, false, MODE, CONV>(maps, fp, a, nz, st);
+        case 64: return bf ? dispatch_flags<64, true, MODE, CONV>(maps, fp, a, nz, st)
+                           : dispatch_flags<64, false, MODE, CONV>(maps, fp, a, nz, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// The conv-prologue instantiations of dispatch<MODE, true> (scan_fast_conv.cu).
+cudaError_t dispatch_conv_full(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz,
+                               cudaStream_t st);
+cudaError_t dispatch_conv_pass1(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz,
+                                cudaStream_t st);
+
+}  // namespace fast
+}  // namespace ssm

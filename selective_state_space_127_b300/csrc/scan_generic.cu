@@ -11,6 +11,9 @@
 // deltaB_u = delta B u, x = deltaA x + deltaB_u, y = x.C, y + u D) and MambaBlock.forward
 // (y * silu(z)); "論文解説: Mamba" "選択機構" (softplus) and "Hardware-Aware Parallel Scan".
 // Exact ZOH: "State Space Model / Mamba" "Zero-Order Hold", `discretize_zoh`.
+// Optional prologue: x replaced by silu(causal depthwise conv1d(x)) with a window of the
+// K - 1 previous raw inputs in registers ("Mamba/SSM complete guide" section 5 `MambaBlock`:
+// conv1d with padding d_conv - 1 cut to L steps, then F.silu).
 #include "common.cuh"
 #include "internal.h"
 
@@ -41,6 +44,16 @@ scan_generic_kernel(const ScanArgs a) {
     }
     const float Dd = (active && a.D) ? a.D[d] : 0.f;
     const float bias = (active && a.bias) ? a.bias[d] : 0.f;
+    // conv prologue: taps right-aligned into cw[0..3] (cw[3] multiplies x_t), win = x_{t-3..t-1}
+    float cw[4] = {0.f, 0.f, 0.f, 0.f}, cb = 0.f, win[3] = {0.f, 0.f, 0.f};
+    if (a.conv_w && active) {
+        const int K = a.conv_k;
+        for (int j = 4 - K; j < 4; ++j) cw[j] = a.conv_w[d * K + j - (4 - K)];
+        cb = a.conv_b ? a.conv_b[d] : 0.f;
+        if (a.conv_prev)
+            for (int m = 1; m < K; ++m)   // x_{-m} = x_prev[b, K-1-m]
+                win[3 - m] = load_f32(a.conv_prev, (b * (K - 1) + (K - 1 - m)) * a.dim + d, a.io_bf16);
+    }
 
     for (int64_t step = 0; step < a.seqlen; ++step) {
         const int64_t t = a.reverse ? a.seqlen - 1 - step : step;
@@ -49,6 +62,13 @@ scan_generic_kernel(const ScanArgs a) {
             xv = load_f32(a.x, b * a.xs[0] + t * a.xs[1] + d * a.xs[2], a.io_bf16);
             dv = load_f32(a.delta, b * a.ds[0] + t * a.ds[1] + d * a.ds[2], a.io_bf16);
             if (a.z) zv = load_f32(a.z, b * a.zs[0] + t * a.zs[1] + d * a.zs[2], a.io_bf16);
+        }
+        if (a.conv_w) {
+            const float v = fmaf(cw[3], xv, fmaf(cw[2], win[2], fmaf(cw[1], win[1], fmaf(cw[0], win[0], cb))));
+            win[0] = win[1];
+            win[1] = win[2];
+            win[2] = xv;
+            xv = silu_accurate(v);
         }
         float dt = dv + bias;
         if (a.softplus) dt = softplus_accurate(dt);

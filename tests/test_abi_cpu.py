@@ -57,7 +57,8 @@ def _c_offsets(struct, fields):
 
 
 @pytest.mark.parametrize("struct,cls", [("ssm_scan_params", binding.ScanParams),
-                                        ("ssd_scan_params", binding.SSDParams)])
+                                        ("ssd_scan_params", binding.SSDParams),
+                                        ("ssm_conv1d_params", binding.Conv1dParams)])
 def test_ctypes_struct_layout_matches_header(tmp_path, struct, cls):
     fields = [f for f, _ in cls._fields_]
     c = tmp_path / "probe.c"
@@ -139,3 +140,49 @@ def test_invalid_ssd_args_are_rejected_before_launch(lib):
 def test_null_params_are_rejected(lib):
     assert lib.ssm_scan_fwd(None, None) == binding.SSM_ERR_INVALID_ARG
     assert lib.ssd_chunk_scan_fwd(None, None) == binding.SSM_ERR_INVALID_ARG
+
+
+def test_conv_prologue_args_are_checked_before_launch(lib):
+    fake = 1 << 20
+    p = _valid_scan_params()
+    p.conv_weight, p.conv_width = fake, 5            # more than 4 taps
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
+    p.conv_width = 0
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
+    p.conv_width, p.reverse = 4, 1                    # the prologue is causal: forward only
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_UNSUPPORTED
+    p.reverse, p.conv_x_prev = 0, fake + 1            # x_prev not aligned to bf16
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
+    p.conv_x_prev, p.reserved2 = 0, 1
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
+    p.reserved2 = 0
+    assert lib.ssm_scan_workspace_size(ctypes.byref(p)) != ctypes.c_size_t(-1).value
+
+
+def _valid_conv_params():
+    p = binding.Conv1dParams()
+    p.batch, p.seqlen, p.dim, p.width = 2, 64, 16, 4
+    p.io_dtype, p.silu = binding.SSM_DTYPE_BF16, 1
+    p.x, p.weight, p.y = 1 << 20, 1 << 21, 1 << 22
+    return p
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("batch", 0, binding.SSM_ERR_INVALID_ARG),
+    ("seqlen", -1, binding.SSM_ERR_INVALID_ARG),
+    ("width", 0, binding.SSM_ERR_INVALID_ARG),
+    ("width", 5, binding.SSM_ERR_INVALID_ARG),
+    ("io_dtype", 3, binding.SSM_ERR_INVALID_ARG),
+    ("silu", 2, binding.SSM_ERR_INVALID_ARG),
+    ("reserved", 1, binding.SSM_ERR_INVALID_ARG),
+    ("weight", 0, binding.SSM_ERR_INVALID_ARG),
+    ("x", (1 << 20) + 8, binding.SSM_ERR_INVALID_ARG),     # not 16-byte aligned
+    ("dim", 12, binding.SSM_ERR_UNSUPPORTED),              # 24 bytes of bf16 per row
+    ("y", (1 << 20) + 1024, binding.SSM_ERR_INVALID_ARG),  # overlaps x
+])
+def test_invalid_conv1d_args_are_rejected_before_launch(lib, field, value, status):
+    p = _valid_conv_params()
+    setattr(p, field, value)
+    assert lib.ssm_causal_conv1d_fwd(ctypes.byref(p), None) == status
+    assert lib.ssm_last_error().decode() != ""
+    assert lib.ssm_causal_conv1d_fwd(None, None) == binding.SSM_ERR_INVALID_ARG
