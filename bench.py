@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--no-ssd", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-conv", action="store_true", help="skip the conv1d + SiLU prologue measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra-workloads", action="store_true", help="also time scan workloads 2 and 3")
     return ap.parse_args()
@@ -267,7 +268,8 @@ def _max_over_ranks(v, dev, world):
 def run_ours(args):
     import torch
     import torch.distributed as dist
-    from selective_state_space_127_b300 import binding, ssd_chunk_scan_fwd, ssm_scan_fwd, ssm_scan_fwd_host
+    from selective_state_space_127_b300 import (binding, causal_conv1d_fwd, ssd_chunk_scan_fwd, ssm_scan_fwd,
+                                                ssm_scan_fwd_host)
     from selective_state_space_127_b300.synth import (SCAN_WORKLOADS, SSD_WORKLOAD, scan_workload_inputs,
                                                       ssd_workload_inputs)
 
@@ -327,7 +329,7 @@ def run_ours(args):
         "hbm_peak_gbs": peaks["hbm_gbs"], "peak_source": peak_src,
         "roofline": {"bound": "alu", "achieved": round(achieved_upd, 1), "peak": round(alu_peak, 1),
                      "unit": "Gupdate/s", "frac": round(achieved_upd / alu_peak, 4),
-                     "traffic": profiled_traffic("scan_fast.cu", "scan_fast_b8_D1536_L2048_N16_bf16.md"),
+                     "traffic": profiled_traffic("scan_fast.cuh", "scan_fast_b8_D1536_L2048_N16_bf16.md"),
                      "kernel": "selective scan", "algorithmic_bytes": nbytes, "updates": updates,
                      "peak_basis": f"{UPDATES_PER_CLK_SM:.0f} updates/clk/SM x {SMS} SMs x {mhz_peak:.0f} MHz "
                                    "(ex2 and FP32-lane limits, measured)"},
@@ -362,6 +364,43 @@ def run_ours(args):
                                       "kernel": "ssd_tc_kernel", "mma_flops_per_launch": mma,
                                       "peak_basis": "measured bf16 dense burst (cuBLAS 8192^3)"}}
         del sinp, sy, shl
+
+    if not args.no_conv:
+        # causal conv1d (4 taps) + SiLU: the standalone kernel on 4x workload 1's x (so that its
+        # input plus output exceed L2), and the scan of workload 1 with the prologue fused
+        K = 4
+        gconv = torch.Generator(device=dev).manual_seed(20261202 + 40 + rank)
+        cw = torch.randn(w.dim, K, generator=gconv, device=dev) / K ** 0.5
+        cb = 0.1 * torch.randn(w.dim, generator=gconv, device=dev)
+        cx = torch.randn(4 * w.batch, w.seqlen, w.dim, generator=gconv, device=dev).to(inp["x"].dtype)
+        cy = torch.empty_like(cx)
+
+        def cstep():
+            causal_conv1d_fwd(cx, cw, cb, silu=True, out=cy)
+
+        csteps = max(3, min(args.steps, 200))
+        cms = _max_over_ranks(_timed(cstep, csteps, max(3, min(args.warmup, 5)), stream, barrier), dev, world)
+        cbytes = 2 * cx.numel() * cx.element_size() + cw.numel() * 4 + cb.numel() * 4
+        cgbs = cbytes / (cms * 1e-3) / 1e9
+        del cx, cy
+
+        def fstep():
+            ssm_scan_fwd(**inp, out=y, h_last=hl, chunk_len=w.chunk_len, workspace=ws, conv_weight=cw, conv_bias=cb)
+
+        fms = _max_over_ranks(_timed(fstep, max(3, min(args.steps, 200)), max(3, min(args.warmup, 5)), stream,
+                                     barrier), dev, world)
+        fbytes = nbytes + cw.numel() * 4 + cb.numel() * 4
+        result["conv1d"] = {
+            "workload": f"causal conv1d K{K} + SiLU, b{4 * w.batch} L{w.seqlen} D{w.dim} {w.dtype} "
+                        "(4x the scan's batch so that in + out > L2)",
+            "ms_per_step": round(cms, 4), "steps": csteps, "value": round(cgbs * world, 1), "unit": "GB/s",
+            "roofline": {"bound": "hbm", "achieved": round(cgbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(cgbs / peaks["hbm_gbs"], 4), "algorithmic_bytes": cbytes,
+                         "traffic": profiled_traffic("conv1d.cu", "conv1d_b32_L2048_D1536_K4_bf16.md"),
+                         "kernel": "conv1d_kernel"},
+            "fused_scan": {"workload": w.name + " with the conv1d + SiLU prologue on x",
+                           "ms_per_step": round(fms, 4), "gbs": round(fbytes / (fms * 1e-3) / 1e9 * world, 1),
+                           "vs_plain_scan": round(fms / ms, 3)}}
 
     if not args.no_decode:
         # single-token recurrent step with the state advanced in place, workload 1's shapes

@@ -7,12 +7,13 @@
 // "Mambaブロックの全体構成" (a d_conv = 4 convolution followed by SiLU).
 //
 // The operation reads x once and writes y once, so it is bound by HBM bandwidth. Each thread
-// owns 16 bytes of channels (8 bf16 or 4 fp32) and a run of kRun consecutive steps: it keeps the
-// K-1 previous inputs of its channels in registers, loads its run's rows with 16-byte
-// non-caching loads (all issued ahead of the arithmetic: the loop is unrolled), and writes 16
-// bytes per step. Consecutive threads take consecutive channel groups of one (b, run), so a
-// warp reads and writes 512 contiguous bytes per step. The K-1 rows before a run are read a
-// second time (by the run that owns them), from L2.
+// owns four channels (8 bytes of bf16, 16 of fp32) and a run of kRun consecutive steps: it keeps
+// the K-1 previous inputs of its channels in registers and walks the run in groups of kSub
+// rows, issuing a group's loads (read-only path) before its arithmetic. Four channels keep the
+// thread within 80 registers, so 24 warps per SM keep 37 KB (bf16) to 74 KB (fp32) of loads in
+// flight. Consecutive threads take consecutive channel groups of one (b, run), so a warp reads and
+// writes 256 (bf16) or 512 (fp32) contiguous bytes per step. The K-1 rows before a run are read
+// a second time (by the run that owns them), from L2.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -22,37 +23,36 @@ namespace ssm {
 namespace {
 
 constexpr int kConvThreads = 256;
-constexpr int kRun = 16;   // steps per thread
+constexpr int kRun = 36;   // steps per thread (six groups)
+constexpr int kSub = 6;    // rows loaded ahead of their arithmetic
 
 template <bool BF16>
 struct Vec;
+// Four channels of one row: the raw load, its widening to fp32, and the rounded store.
 template <>
 struct Vec<true> {
-    static constexpr int kN = 8;
-    static __device__ __forceinline__ void load(const void* p, float (&v)[8]) {
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[2 * i] = __uint_as_float(w[i] << 16);
-            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
+    static constexpr int kN = 4;
+    using Raw = uint2;
+    static __device__ __forceinline__ Raw load(const void* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
+    static __device__ __forceinline__ void widen(Raw q, float (&v)[4]) {
+        v[0] = __uint_as_float(q.x << 16);
+        v[1] = __uint_as_float(q.x & 0xffff0000u);
+        v[2] = __uint_as_float(q.y << 16);
+        v[3] = __uint_as_float(q.y & 0xffff0000u);
     }
-    static __device__ __forceinline__ void store(void* p, const float (&v)[8]) {
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-            w[i] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    static __device__ __forceinline__ void store(void* p, const float (&v)[4]) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(v[2], v[3]);
+        *reinterpret_cast<uint2*>(p) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
     }
 };
 template <>
 struct Vec<false> {
     static constexpr int kN = 4;
-    static __device__ __forceinline__ void load(const void* p, float (&v)[4]) {
-        const float4 q = __ldg(reinterpret_cast<const float4*>(p));
+    using Raw = float4;
+    static __device__ __forceinline__ Raw load(const void* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+    static __device__ __forceinline__ void widen(Raw q, float (&v)[4]) {
         v[0] = q.x;
         v[1] = q.y;
         v[2] = q.z;
@@ -64,7 +64,7 @@ struct Vec<false> {
 };
 
 template <bool BF16, int K, bool SILU>
-__global__ void __launch_bounds__(kConvThreads)
+__global__ void __launch_bounds__(kConvThreads, 3)
 conv1d_kernel(const void* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
               const void* __restrict__ x_prev, void* __restrict__ y, int64_t batch, int64_t L, int64_t dim) {
     using V = Vec<BF16>;
@@ -95,41 +95,48 @@ conv1d_kernel(const void* __restrict__ x, const float* __restrict__ w, const flo
     for (int j = 0; j < K - 1; ++j) {
         const int64_t tt = t0 - (K - 1) + j;
         if (tt >= 0) {
-            V::load(xb + tt * dim * kEsz, win[j]);
+            V::widen(V::load(xb + tt * dim * kEsz), win[j]);
         } else if (x_prev) {
             // x_prev[b, K-1+tt, :] is x_{tt}
-            V::load(static_cast<const char*>(x_prev) + ((b * (K - 1) + (K - 1) + tt) * dim + d0) * kEsz, win[j]);
+            V::widen(V::load(static_cast<const char*>(x_prev) + ((b * (K - 1) + (K - 1) + tt) * dim + d0) * kEsz),
+                     win[j]);
         } else {
 #pragma unroll
             for (int e = 0; e < E; ++e) win[j][e] = 0.f;
         }
     }
     const int nt = (int)(L - t0 < kRun ? L - t0 : kRun);
-    float xs[kRun][E];
+#pragma unroll 1
+    for (int i0 = 0; i0 < nt; i0 += kSub) {
+        typename V::Raw raw[kSub];
 #pragma unroll
-    for (int i = 0; i < kRun; ++i)
-        if (i < nt) V::load(xb + (t0 + i) * dim * kEsz, xs[i]);
+        for (int i = 0; i < kSub; ++i)
+            if (i0 + i < nt) raw[i] = V::load(xb + (t0 + i0 + i) * dim * kEsz);
 #pragma unroll
-    for (int i = 0; i < kRun; ++i) {
-        if (i < nt) {
-            float out[E];
+        for (int i = 0; i < kSub; ++i) {
+            if (i0 + i < nt) {
+                float xv[E], out[E];
+                V::widen(raw[i], xv);
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                float v = fmaf(wk[K - 1][e], xs[i][e], bv[e]);
+                for (int e = 0; e < E; ++e) {
+                    float v = fmaf(wk[K - 1][e], xv[e], bv[e]);
 #pragma unroll
-                for (int j = 0; j < K - 1; ++j) v = fmaf(wk[j][e], win[j][e], v);
-                out[e] = SILU ? silu_accurate(v) : v;
+                    for (int j = 0; j < K - 1; ++j) v = fmaf(wk[j][e], win[j][e], v);
+                    // silu from the SFU's ex2 and rcp (a few ulp): the kernel stays bound by
+                    // memory, not by instruction issue
+                    out[e] = SILU ? silu_fast(v) : v;
+                }
+                V::store(yb + (t0 + i0 + i) * dim * kEsz, out);
+                // slide the window
+#pragma unroll
+                for (int j = 0; j + 1 < K - 1; ++j)
+#pragma unroll
+                    for (int e = 0; e < E; ++e) win[j][e] = win[j + 1][e];
+                if constexpr (K > 1) {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) win[K - 2][e] = xv[e];
+                }
             }
-            V::store(yb + (t0 + i) * dim * kEsz, out);
-        }
-        // slide the window
-#pragma unroll
-        for (int j = 0; j + 1 < K - 1; ++j)
-#pragma unroll
-            for (int e = 0; e < E; ++e) win[j][e] = win[j + 1][e];
-        if constexpr (K > 1) {
-#pragma unroll
-            for (int e = 0; e < E; ++e) win[K - 2][e] = xs[i][e];
         }
     }
 }
