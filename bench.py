@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-conv", action="store_true", help="skip the conv1d + SiLU prologue measurements")
+    ap.add_argument("--no-variants", action="store_true", help="skip the exact-ZOH and reverse measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra-workloads", action="store_true", help="also time scan workloads 2 and 3")
     return ap.parse_args()
@@ -401,6 +402,17 @@ def run_ours(args):
             "fused_scan": {"workload": w.name + " with the conv1d + SiLU prologue on x",
                            "ms_per_step": round(fms, 4), "gbs": round(fbytes / (fms * 1e-3) / 1e9 * world, 1),
                            "vs_plain_scan": round(fms / ms, 3)}}
+
+    if not args.no_variants:
+        # the exact-ZOH discretisation and the reverse direction on workload 1 (generic kernel)
+        variants = {}
+        for name, kw in (("zoh", {"zoh": True}), ("reverse", {"reverse": True})):
+            def vstep(kw=kw):
+                ssm_scan_fwd(**inp, out=y, h_last=hl, **kw)
+            vms = _max_over_ranks(_timed(vstep, max(3, min(args.steps, 20)), 3, stream, barrier), dev, world)
+            variants[name] = {"ms_per_step": round(vms, 4), "gbs": round(nbytes / (vms * 1e-3) / 1e9 * world, 1),
+                              "kernel": "scan_generic_kernel"}
+        result["variants"] = dict(workload=w.name, **variants)
 
     if not args.no_decode:
         # single-token recurrent step with the state advanced in place, workload 1's shapes
