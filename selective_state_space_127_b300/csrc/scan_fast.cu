@@ -1,6 +1,9 @@
 // Fast selective-scan kernels for dense channel-contiguous layouts (the Mamba block's
-// (b, L, D) activations and (b, L, N) B, C), N in {16, 32, 64}, forward direction,
-// delta*B discretisation; with an optional split of the sequence into chunks.
+// (b, L, D) activations and (b, L, N) B, C), N in {16, 32, 64}, delta*B discretisation, with
+// an optional split of the sequence into chunks; variants (one per kernel) add the conv1d +
+// SiLU prologue on x, the exact zero-order hold B_bar = (A_bar - 1) / A B (a series in
+// z = dt A for |z| < 1/8, where the difference would cancel), or walk the sequence backwards
+// (tiles in reverse order, rows of a tile from last to first; one chunk).
 //
 // Work split. A CTA owns kCh = 16 consecutive channels of one batch row and walks one
 // chunk of the sequence (the whole sequence when it is not split). LPC lanes share a
@@ -109,7 +112,8 @@ constexpr int64_t kMinChunk = 512;    // shortest chunk the automatic split uses
 bool scan_fast_supported(const ScanArgs& a) {
     const int N = a.dstate;
     if (N != 16 && N != 32 && N != 64) return false;
-    if (a.reverse || a.zoh) return false;
+    // one variant per kernel: the conv prologue, exact ZOH or the reverse direction
+    if ((a.conv_w != nullptr) + a.zoh + a.reverse > 1) return false;
     if (a.batch > 65535 || a.dim > (int64_t)1 << 30 || a.seqlen > ((int64_t)1 << 31) - 2 * kT) return false;
     if (!encode_fn()) return false;
     const int64_t esz = a.io_bf16 ? 2 : 4;
@@ -132,6 +136,7 @@ bool scan_fast_supported(const ScanArgs& a) {
 
 int64_t scan_fast_chunk(const ScanArgs& a) {
     const int64_t L = a.seqlen;
+    if (a.reverse) return ((L + kT - 1) / kT) * kT;   // the reverse kernel walks one chunk
     int64_t q;
     if (a.chunk_len > 0) {
         q = a.chunk_len;
@@ -180,8 +185,9 @@ cudaError_t launch_scan_fast(const ScanArgs& a, cudaStream_t st) {
         const size_t carry_floats = (size_t)((nch - 1) * a.batch * a.dim * a.dstate);
         fp.carry = static_cast<float*>(a.workspace);
         fp.sumdt = fp.carry + carry_floats;
-        cudaError_t e = conv ? dispatch_conv_pass1(maps, fp, a, nch - 1, st)
-                             : dispatch<kPass1, false>(maps, fp, a, nch - 1, st);
+        cudaError_t e = conv     ? dispatch_conv_pass1(maps, fp, a, nch - 1, st)
+                        : a.zoh ? dispatch_zoh_pass1(maps, fp, a, nch - 1, st)
+                                : dispatch<kPass1, kVarPlain>(maps, fp, a, nch - 1, st);
         if (e != cudaSuccess) return e;
         const int64_t total = a.batch * a.dim * a.dstate;
         scan_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(fp.carry, fp.sumdt, a.A, a.h0, a.batch,
@@ -190,7 +196,10 @@ cudaError_t launch_scan_fast(const ScanArgs& a, cudaStream_t st) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    return conv ? dispatch_conv_full(maps, fp, a, nch, st) : dispatch<kFull, false>(maps, fp, a, nch, st);
+    if (conv) return dispatch_conv_full(maps, fp, a, nch, st);
+    if (a.zoh) return dispatch_zoh_full(maps, fp, a, nch, st);
+    if (a.reverse) return dispatch_rev_full(maps, fp, a, nch, st);
+    return dispatch<kFull, kVarPlain>(maps, fp, a, nch, st);
 }
 
 }  // namespace ssm

@@ -45,8 +45,13 @@ struct FastParams {
 // Rows of x before a tile that the conv prologue reads (the widest kernel, 4 taps, needs 3).
 constexpr int kHalo = 3;
 
-template <int N, bool BF16, bool CONV>
+// Kernel variants: plain; conv1d + SiLU prologue on x; exact zero-order hold
+// B_bar = (A_bar - 1) / A B; the sequence walked from t = L-1 down to 0 (one chunk only).
+enum Variant { kVarPlain = 0, kVarConv = 1, kVarZoh = 2, kVarRev = 3 };
+
+template <int N, bool BF16, int VAR>
 struct Layout {
+    static constexpr bool CONV = VAR == kVarConv;
     static constexpr int kEsz = BF16 ? 2 : 4;
     static constexpr int kTileX = kT * kCh * kEsz;          // one of x, delta, z, y
     static constexpr int kTileB = kT * N * kEsz;            // one of B, C
@@ -81,12 +86,13 @@ struct ConvTaps {
     float b;
 };
 
-template <bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS, bool CONV>
+// With VAR == kVarZoh, u carries x itself (the ZOH input coefficient depends on the state).
+template <bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS, int VAR>
 __device__ __forceinline__ Scal scalars(const void* xs, const void* ds, const void* zs, int jj, int c, float bias,
                                         float Dd, bool tv, const ConvTaps& ct) {
     Scal r;
     float xr;
-    if constexpr (CONV) {
+    if constexpr (VAR == kVarConv) {
         // the x tile starts kHalo rows early: rows jj .. jj + 3 hold x_{t-3} .. x_t
         float v = ct.b;
 #pragma unroll
@@ -98,7 +104,7 @@ __device__ __forceinline__ Scal scalars(const void* xs, const void* ds, const vo
     float dt = ld_io(ds, jj * kCh + c, BF16) + bias;
     if constexpr (SOFTPLUS) dt = softplus_fast(dt);
     r.dt = tv ? dt : 0.f;
-    r.u = r.dt * xr;
+    r.u = VAR == kVarZoh ? (tv ? xr : 0.f) : r.dt * xr;
     r.dx = DSKIP ? Dd * xr : 0.f;
     r.gate = GATE ? silu_fast(ld_io(zs, jj * kCh + c, BF16)) : 1.f;
     return r;
@@ -120,13 +126,16 @@ __device__ __forceinline__ void lds_pairs(const float* p, f2 (&v)[S / 2]) {
     }
 }
 
-template <int N, bool BF16, int LPC, bool GATE, bool DSKIP, bool SOFTPLUS, int MODE, bool CONV>
+template <int N, bool BF16, int LPC, bool GATE, bool DSKIP, bool SOFTPLUS, int MODE, int VAR>
 __global__ void __launch_bounds__(kCh * LPC, 16 / LPC)
 scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap md,
                  const __grid_constant__ CUtensorMap mz, const __grid_constant__ CUtensorMap mB,
                  const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap my,
                  const FastParams p) {
-    using Lay = Layout<N, BF16, CONV>;
+    using Lay = Layout<N, BF16, VAR>;
+    constexpr bool CONV = VAR == kVarConv;
+    constexpr bool ZOH = VAR == kVarZoh;
+    constexpr bool REV = VAR == kVarRev;   // one chunk only
     constexpr int kThreads = kCh * LPC;
     constexpr int S = N / LPC;         // states per lane
     constexpr int P = S / 2;           // packed pairs per lane
@@ -159,19 +168,21 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
             hinit = p.carry + ((int64_t)(chunk - 1) * gridDim.y + b) * p.dim * N;
     }
     f2 A2[P], h[P];
+    f2 Ainv[ZOH ? P : 1];   // ZOH: 1 / A (0 where A == 0)
 #pragma unroll
     for (int k = 0; k < P; ++k) {
         const int n = g * S + 2 * k;
         float a0 = 0.f, a1 = 0.f, h0v = 0.f, h1v = 0.f;
         if (dvalid) {
-            a0 = p.A[(int64_t)d * N + n] * kLog2e;
-            a1 = p.A[(int64_t)d * N + n + 1] * kLog2e;
+            a0 = p.A[(int64_t)d * N + n];
+            a1 = p.A[(int64_t)d * N + n + 1];
             if (hinit) {
                 h0v = hinit[(int64_t)d * N + n];
                 h1v = hinit[(int64_t)d * N + n + 1];
             }
         }
-        A2[k] = pk(a0, a1);
+        if constexpr (ZOH) Ainv[k] = pk(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
+        A2[k] = pk(a0 * kLog2e, a1 * kLog2e);
         h[k] = pk(h0v, h1v);
     }
     const float bias = (dvalid && p.bias) ? p.bias[d] : 0.f;
@@ -195,7 +206,7 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         constexpr unsigned kBytes =
             Lay::kXBox + Lay::kTileX + (kGate ? Lay::kTileX : 0) + Lay::kTileB + (kReadout ? Lay::kTileB : 0);
         mbar_arrive_expect_tx(&bars[buf], kBytes);
-        const int t0 = (int)(t_begin + (int64_t)s * kT);
+        const int t0 = (int)(t_begin + (int64_t)(REV ? ntiles - 1 - s : s) * kT);
         // with the conv prologue the x box starts kHalo rows early (zero-filled before t = 0)
         tma_load_3d(st, &mx, d0, CONV ? t0 - kHalo : t0, b, &bars[buf]);
         tma_load_3d(st + Lay::kOffD, &md, d0, t0, b, &bars[buf]);
@@ -274,18 +285,22 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         unsigned char* ys = smem + Lay::kY + (s & 1) * Lay::kYStride;
         if (kReadout && s >= 2 && tid == 0) tma_store_wait_read<1>();   // the store of tile s-2 read ys
         __syncthreads();
-        const int rem = (int)(len - (int64_t)s * kT);
+        const int ts = REV ? ntiles - 1 - s : s;   // the tile's index in time order
+        const int rem = (int)(len - (int64_t)ts * kT);
         const int tcount = rem < kT ? rem : kT;
+        // processing step k of the tile is its row rr(k): the rows run backwards in reverse
+        auto rr = [](int k) { return REV ? kT - 1 - k : k; };
 
         float yout[kT / LPC];   // the steps this lane finishes; stored after the loop so that no
                                 // shared-memory store sits between the loads of later steps
-        Scal cur = scalars<BF16, kGate, DSKIP && kReadout, SOFTPLUS, CONV>(xs, ds, zs, g, c, bias, Dd, g < tcount, ct);
+        Scal cur = scalars<BF16, kGate, DSKIP && kReadout, SOFTPLUS, VAR>(xs, ds, zs, rr(g), c, bias, Dd,
+                                                                          rr(g) < tcount, ct);
 #pragma unroll
         for (int grp = 0; grp < kT / LPC; ++grp) {
             // the next group's scalars: independent of the state, overlaps the updates below
             const int jn = (grp + 1) * LPC + g;
-            const Scal nxt = scalars<BF16, kGate, DSKIP && kReadout, SOFTPLUS, CONV>(
-                xs, ds, zs, jn < kT ? jn : g, c, bias, Dd, jn < tcount, ct);
+            const Scal nxt = scalars<BF16, kGate, DSKIP && kReadout, SOFTPLUS, VAR>(
+                xs, ds, zs, jn < kT ? rr(jn) : rr(g), c, bias, Dd, jn < kT && rr(jn) < tcount, ct);
             float acc[LPC];
 #pragma unroll
             for (int q = 0; q < LPC; ++q) {
@@ -293,17 +308,38 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
                 const float uq = __shfl_sync(0xffffffffu, cur.u, q, LPC);
                 if constexpr (MODE == kPass1) dtsum += dtq;
                 const f2 dt2 = pk(dtq, dtq), u2 = pk(uq, uq);
+                const int row = rr(grp * LPC + q);
                 f2 bv[P];
-                lds_pairs<S>(Bf + (grp * LPC + q) * N + g * S, bv);
+                lds_pairs<S>(Bf + row * N + g * S, bv);
                 f2 cv[P];
-                if constexpr (kReadout) lds_pairs<S>(Cf + (grp * LPC + q) * N + g * S, cv);
+                if constexpr (kReadout) lds_pairs<S>(Cf + row * N + g * S, cv);
                 f2 a2 = pk(0.f, 0.f);
 #pragma unroll
                 for (int k = 0; k < P; ++k) {
                     float e0, e1;
-                    upk(mul2(dt2, A2[k]), e0, e1);
+                    const f2 e2 = mul2(dt2, A2[k]);   // dt A log2 e
+                    upk(e2, e0, e1);
                     const f2 ab = pk(ex2_approx(e0), ex2_approx(e1));
-                    h[k] = fma2(ab, h[k], mul2(u2, bv[k]));
+                    f2 ub;
+                    if constexpr (ZOH) {
+                        // B_bar x = c B x with c = (A_bar - 1) / A; for |z| = |dt A| < 1/8 the
+                        // series dt (1 + z/2 + z^2/6 + z^3/24 + z^4/120) (no cancellation; the
+                        // dropped z^5/720 term is below 5e-8 relative), else (A_bar - 1) (1 / A)
+                        const f2 z2 = mul2(e2, pk(kLn2, kLn2));
+                        f2 sr = fma2(z2, pk(1.f / 120.f, 1.f / 120.f), pk(1.f / 24.f, 1.f / 24.f));
+                        sr = fma2(z2, sr, pk(1.f / 6.f, 1.f / 6.f));
+                        sr = fma2(z2, sr, pk(0.5f, 0.5f));
+                        sr = fma2(z2, sr, pk(1.f, 1.f));
+                        float z0, z1, s0, s1, b0, b1;
+                        upk(z2, z0, z1);
+                        upk(mul2(dt2, sr), s0, s1);
+                        upk(mul2(fma2(ab, pk(1.f, 1.f), pk(-1.f, -1.f)), Ainv[k]), b0, b1);
+                        const f2 coef = pk(fabsf(z0) < 0.125f ? s0 : b0, fabsf(z1) < 0.125f ? s1 : b1);
+                        ub = mul2(mul2(coef, u2), bv[k]);
+                    } else {
+                        ub = mul2(u2, bv[k]);
+                    }
+                    h[k] = fma2(ab, h[k], ub);
                     if constexpr (kReadout) a2 = fma2(cv[k], h[k], a2);
                 }
                 if constexpr (kReadout) {
@@ -333,7 +369,7 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         if constexpr (kReadout) {
 #pragma unroll
             for (int grp = 0; grp < kT / LPC; ++grp) {
-                const int jj = grp * LPC + g;
+                const int jj = rr(grp * LPC + g);
                 if constexpr (BF16)
                     reinterpret_cast<__nv_bfloat16*>(ys)[jj * kCh + c] = __float2bfloat16_rn(yout[grp]);
                 else
@@ -344,7 +380,7 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         __syncthreads();
         if (tid == 0) {
             if constexpr (kReadout) {
-                tma_store_3d(&my, d0, (int)(t_begin + (int64_t)s * kT), b, ys);
+                tma_store_3d(&my, d0, (int)(t_begin + (int64_t)ts * kT), b, ys);
                 tma_store_commit();
             }
             if (s + kStages < ntiles) issue(s + kStages);
@@ -382,11 +418,11 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
 template <int N>
 constexpr int lanes_per_channel() { return N / 8; }
 
-template <int N, bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS, int MODE, bool CONV,
+template <int N, bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS, int MODE, int VAR,
           int LPC = lanes_per_channel<N>()>
 cudaError_t launch_t(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz, cudaStream_t st) {
-    using Lay = Layout<N, BF16, CONV>;
-    auto kern = scan_fast_kernel<N, BF16, LPC, GATE, DSKIP, SOFTPLUS, MODE, CONV>;
+    using Lay = Layout<N, BF16, VAR>;
+    auto kern = scan_fast_kernel<N, BF16, LPC, GATE, DSKIP, SOFTPLUS, MODE, VAR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kTotal);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.dim + kCh - 1) / kCh), (unsigned)a.batch, (unsigned)nz);
@@ -395,16 +431,16 @@ cudaError_t launch_t(const CUtensorMap* maps, const FastParams& fp, const ScanAr
     return cudaGetLastError();
 }
 
-template <int N, bool BF16, int MODE, bool CONV>
+template <int N, bool BF16, int MODE, int VAR>
 cudaError_t dispatch_flags(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz, cudaStream_t st) {
     const bool gate = a.z != nullptr, dskip = a.D != nullptr, sp = a.softplus != 0;
     if constexpr (MODE == kPass1) {
         // pass 1 reads neither z nor D
-        return sp ? launch_t<N, BF16, false, false, true, MODE, CONV>(maps, fp, a, nz, st)
-                  : launch_t<N, BF16, false, false, false, MODE, CONV>(maps, fp, a, nz, st);
+        return sp ? launch_t<N, BF16, false, false, true, MODE, VAR>(maps, fp, a, nz, st)
+                  : launch_t<N, BF16, false, false, false, MODE, VAR>(maps, fp, a, nz, st);
     } else {
 #define SSM_FAST_CASE(G_, D_, S_) \
-    if (gate == G_ && dskip == D_ && sp == S_) return launch_t<N, BF16, G_, D_, S_, MODE, CONV>(maps, fp, a, nz, st);
+    if (gate == G_ && dskip == D_ && sp == S_) return launch_t<N, BF16, G_, D_, S_, MODE, VAR>(maps, fp, a, nz, st);
         SSM_FAST_CASE(true, true, true)
         SSM_FAST_CASE(true, true, false)
         SSM_FAST_CASE(true, false, true)
@@ -418,25 +454,32 @@ cudaError_t dispatch_flags(const CUtensorMap* maps, const FastParams& fp, const 
     return cudaErrorInvalidValue;
 }
 
-template <int MODE, bool CONV>
+template <int MODE, int VAR>
 cudaError_t dispatch(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz, cudaStream_t st) {
     const bool bf = a.io_bf16 != 0;
     switch (a.dstate) {
-        case 16: return bf ? dispatch_flags<16, true, MODE, CONV>(maps, fp, a, nz, st)
-                           : dispatch_flags<16, false, MODE, CONV>(maps, fp, a, nz, st);
-        case 32: return bf ? dispatch_flags<32, true, MODE, CONV>(maps, fp, a, nz, st)
-                           : dispatch_flags<32, false, MODE, CONV>(maps, fp, a, nz, st);
-        case 64: return bf ? dispatch_flags<64, true, MODE, CONV>(maps, fp, a, nz, st)
-                           : dispatch_flags<64, false, MODE, CONV>(maps, fp, a, nz, st);
+        case 16: return bf ? dispatch_flags<16, true, MODE, VAR>(maps, fp, a, nz, st)
+                           : dispatch_flags<16, false, MODE, VAR>(maps, fp, a, nz, st);
+        case 32: return bf ? dispatch_flags<32, true, MODE, VAR>(maps, fp, a, nz, st)
+                           : dispatch_flags<32, false, MODE, VAR>(maps, fp, a, nz, st);
+        case 64: return bf ? dispatch_flags<64, true, MODE, VAR>(maps, fp, a, nz, st)
+                           : dispatch_flags<64, false, MODE, VAR>(maps, fp, a, nz, st);
     }
     return cudaErrorInvalidValue;
 }
 
-// The conv-prologue instantiations of dispatch<MODE, true> (scan_fast_conv.cu).
+// The instantiations of the other variants, each in a translation unit of its own:
+// conv prologue (scan_fast_conv.cu), exact ZOH and reverse (scan_fast_var.cu).
 cudaError_t dispatch_conv_full(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz,
                                cudaStream_t st);
 cudaError_t dispatch_conv_pass1(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz,
                                 cudaStream_t st);
+cudaError_t dispatch_zoh_full(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz,
+                              cudaStream_t st);
+cudaError_t dispatch_zoh_pass1(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz,
+                               cudaStream_t st);
+cudaError_t dispatch_rev_full(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz,
+                              cudaStream_t st);
 
 }  // namespace fast
 }  // namespace ssm

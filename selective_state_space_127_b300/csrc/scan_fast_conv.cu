@@ -7,12 +7,12 @@ namespace fast {
 
 cudaError_t dispatch_conv_full(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz,
                                cudaStream_t st) {
-    return dispatch<kFull, true>(maps, fp, a, nz, st);
+    return dispatch<kFull, kVarConv>(maps, fp, a, nz, st);
 }
 
 cudaError_t dispatch_conv_pass1(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz,
                                 cudaStream_t st) {
-    return dispatch<kPass1, true>(maps, fp, a, nz, st);
+    return dispatch<kPass1, kVarConv>(maps, fp, a, nz, st);
 }
 
 }  // namespace fast

@@ -135,3 +135,44 @@ def test_automatic_split_for_few_channels(cuda_dev):
     assert rel_l2(y.float().cpu().numpy(), y_ref) <= TOL_Y["bf16"]
     assert rel_l2(h.cpu().numpy(), h_ref) <= TOL_H["bf16"]
     assert binding.scan_workspace_size(**g) > 0
+
+
+VARIANT_CASES = [
+    # b, L, D, N, dtype, zoh, reverse, chunk_len, with h0
+    (2, 77, 40, 16, "bf16", True, False, 0, True),
+    (1, 300, 48, 64, "f32", True, False, 0, False),
+    (2, 129, 24, 32, "f32", True, False, 0, True),
+    (1, 1000, 32, 16, "f32", True, False, 96, True),    # ZOH through the chunked path
+    (2, 77, 40, 16, "bf16", False, True, 0, True),
+    (1, 300, 48, 64, "f32", False, True, 0, False),
+    (3, 129, 24, 32, "f32", False, True, 0, True),
+    (1, 4096, 16, 16, "bf16", False, True, 0, False),   # would be split forward; reverse is one chunk
+]
+
+
+@pytest.mark.parametrize("b,L,D,N,dt,zoh,rev,q,with_h0", VARIANT_CASES)
+def test_zoh_and_reverse_on_the_tma_path(cuda_dev, b, L, D, N, dt, zoh, rev, q, with_h0):
+    """Exact-ZOH and reverse-direction kernels of the TMA path against the oracle and the
+    generic kernel (forced by a misaligned copy of x)."""
+    A = None
+    if zoh:
+        # A with zeros (the dt B limit), tiny and large magnitudes: both branches of the
+        # ZOH coefficient (series for |dt A| < 1/8, (A_bar - 1) / A above)
+        row = -torch.logspace(-4, 1.5, N, dtype=torch.float64)
+        row[::5] = 0.0
+        A = row.to(torch.float32).repeat(D, 1)
+    inp = make_scan_inputs(b, L, D, N, dt, seed=7000 + L + D + N + 2 * zoh + rev, d_skip="normal", A=A)
+    h0 = torch.randn(b, D, N, generator=torch.Generator().manual_seed(L + 1)) if with_h0 else None
+    g = _to(cuda_dev, inp)
+    h0_d = h0.to(cuda_dev) if h0 is not None else None
+    y_f, h_f = ssm_scan_fwd(**g, h0=h0_d, zoh=zoh, reverse=rev, chunk_len=q)
+    y_g, h_g = ssm_scan_fwd(**dict(g, x=_misaligned_copy(g["x"])), h0=h0_d, zoh=zoh, reverse=rev)
+    torch.cuda.synchronize()
+    y_ref, h_ref = oracle.ssm_scan_ref(**inp, h0=h0, zoh=zoh, reverse=rev)
+    assert rel_l2(y_f.float().cpu().numpy(), y_ref) <= TOL_Y[dt]
+    assert rel_l2(h_f.cpu().numpy(), h_ref) <= TOL_H[dt]
+    assert rel_l2(y_g.float().cpu().numpy(), y_ref) <= TOL_Y[dt]
+    assert rel_l2(h_f.cpu().numpy(), h_g.cpu().numpy()) <= 1e-5
+    if rev:
+        assert binding.scan_workspace_size(**g, reverse=True) == 0
+    assert device_status() == binding.SSM_OK
