@@ -114,10 +114,11 @@ typedef struct ssm_scan_params {
     int64_t B_stride[3];    /* (b, t, n) */
     int64_t C_stride[3];
     int64_t chunk_len;      /* steps per chunk when the sequence is split across CTAs (the TMA
-                               path rounds it up to a multiple of 16; >= L or a path that does
-                               not split: one chunk); 0 = let the library choose. The result does
-                               not depend on it beyond fp32 rounding. With more than one chunk the
-                               call needs (nchunks - 1) * b * D * (N + 1) * 4 bytes of workspace. */
+                               path rounds it up to a multiple of 32 and to at least L / 65535;
+                               >= L, the reverse direction, or a path that does not split: one
+                               chunk); 0 = let the library choose. The result does not depend on
+                               it beyond fp32 rounding. With more than one chunk the call needs
+                               (nchunks - 1) * b * D * (N + 1) * 4 bytes of workspace. */
     void* workspace;        /* device scratch of ssm_scan_workspace_size() bytes, 256-byte
                                aligned; may be NULL when that size is 0 */
     size_t workspace_bytes;

@@ -106,6 +106,7 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int64_t inner, int64_
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 constexpr int64_t kMinChunk = 512;    // shortest chunk the automatic split uses
+constexpr int64_t kMaxChunks = 65535; // the grid's z extent
 
 }  // namespace
 
@@ -149,6 +150,9 @@ int64_t scan_fast_chunk(const ScanArgs& a) {
         q = (L + nch - 1) / nch;
         if (q < kMinChunk) q = kMinChunk;
     }
+    // at most kMaxChunks chunks: the chunk index is the grid's z dimension
+    const int64_t min_q = (L + kMaxChunks - 1) / kMaxChunks;
+    if (q < min_q) q = min_q;
     q = ((q + kT - 1) / kT) * kT;
     if (q >= L) q = ((L + kT - 1) / kT) * kT;
     return q;

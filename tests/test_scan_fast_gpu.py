@@ -176,3 +176,19 @@ def test_zoh_and_reverse_on_the_tma_path(cuda_dev, b, L, D, N, dt, zoh, rev, q, 
     if rev:
         assert binding.scan_workspace_size(**g, reverse=True) == 0
     assert device_status() == binding.SSM_OK
+
+
+def test_tiny_chunk_len_on_a_long_sequence_is_capped_at_the_grid_limit(cuda_dev):
+    """chunk_len = 32 on 2.2 M steps would need more than 65535 chunks (the grid's z extent):
+    the library lengthens the chunks and the result still matches the oracle."""
+    L = 2_200_000
+    inp = make_scan_inputs(1, L, 16, 16, "bf16", seed=4343, d_skip="normal")
+    g = _to(cuda_dev, inp)
+    ws = binding.scan_workspace_size(**g, chunk_len=32)
+    assert 0 < ws <= 65534 * 16 * 17 * 4
+    y, h = ssm_scan_fwd(**g, chunk_len=32)
+    torch.cuda.synchronize()
+    y_ref, h_ref = oracle.ssm_scan_ref(**inp)
+    assert rel_l2(y[:, -20000:].float().cpu().numpy(), y_ref[:, -20000:]) <= TOL_Y["bf16"]
+    assert rel_l2(h.cpu().numpy(), h_ref) <= TOL_H["bf16"]
+    assert device_status() == binding.SSM_OK
