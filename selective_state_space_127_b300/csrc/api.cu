@@ -200,8 +200,9 @@ ssm_status_t validate_conv1d(const ssm_conv1d_params* p, ssm::Conv1dArgs* out) {
     return SSM_OK;
 }
 
-// Sequences this short (a decode step is L = 1) take the generic kernel: one launch, no
-// TMA tile set-up, the state read once and written once (in place when h0 == h_last).
+// Sequences this short (a decode step is L = 1) take the short-sequence kernel (or the generic
+// one for layouts it does not take): one launch, no TMA tile set-up, the state read once and
+// written once (in place when h0 == h_last).
 constexpr int64_t kShortSeq = 4;
 
 size_t scan_workspace_bytes(const ssm::ScanArgs& a) {
@@ -302,6 +303,8 @@ ssm_status_t ssm_scan_fwd(const ssm_scan_params* p, void* stream) {
         }
     } else if (a.seqlen > kShortSeq && ssm::scan_fast_supported(a)) {
         e = ssm::launch_scan_fast(a, st);
+    } else if (a.seqlen <= kShortSeq && ssm::scan_decode_supported(a)) {
+        e = ssm::launch_scan_decode(a, st);
     } else {
         e = ssm::launch_scan_generic(a, st);
     }

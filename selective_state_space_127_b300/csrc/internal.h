@@ -84,6 +84,8 @@ cudaError_t read_device_status(unsigned* out, bool clear, cudaStream_t st);
 
 // Kernel launchers: return cudaSuccess or the launch error. They assume valid args.
 cudaError_t launch_conv1d(const Conv1dArgs& a, cudaStream_t st);
+bool scan_decode_supported(const ScanArgs& a);
+cudaError_t launch_scan_decode(const ScanArgs& a, cudaStream_t st);
 cudaError_t launch_scan_generic(const ScanArgs& a, cudaStream_t s);
 bool scan_fast_supported(const ScanArgs& a);
 // Steps per chunk the fast path uses (a multiple of its tile; >= seqlen when not split) and

@@ -227,3 +227,43 @@ def test_decode_steps_advance_the_state_in_place(cuda_dev, dt):
     y_ref, h_ref = oracle.ssm_scan_ref(**inp, h0=h0)
     assert rel_l2(torch.cat(ys, 1).float().cpu().numpy(), y_ref) <= TOL_Y[dt]
     assert rel_l2(state.cpu().numpy(), h_ref) <= TOL_H[dt]
+
+
+def _misaligned_A(A):
+    """The same A in a buffer offset by one float (not 16-byte aligned): the short-sequence
+    kernel refuses it and the generic kernel runs."""
+    big = torch.empty(A.numel() + 1, dtype=A.dtype, device=A.device)
+    v = big[1:].view(A.shape)
+    v.copy_(A)
+    return v
+
+
+SHORT_CASES = [
+    # b, L, D, N, dtype, zoh, reverse, with h0
+    (3, 1, 40, 16, "bf16", False, False, True),
+    (2, 2, 24, 4, "f32", False, False, False),
+    (2, 3, 17, 8, "f32", True, False, True),
+    (1, 4, 33, 32, "bf16", False, True, True),
+    (2, 1, 8, 64, "f32", True, True, True),
+    (1, 4, 5, 128, "f32", False, False, True),
+    (2, 1, 16, 12, "f32", False, False, True),    # N / 4 = 3: the generic kernel
+]
+
+
+@pytest.mark.parametrize("b,L,D,N,dt,zoh,rev,with_h0", SHORT_CASES)
+def test_short_sequence_kernel_matches_oracle_and_generic(cuda_dev, b, L, D, N, dt, zoh, rev, with_h0):
+    """L <= 4 (the decode step above all) on the short-sequence kernel, against the oracle and
+    against the generic kernel."""
+    inp = make_scan_inputs(b, L, D, N, dt, seed=8100 + L + D + N, d_skip="normal")
+    h0 = torch.randn(b, D, N, generator=torch.Generator().manual_seed(N)) if with_h0 else None
+    g = _to(cuda_dev, inp)
+    h0_d = h0.to(cuda_dev) if h0 is not None else None
+    y_s, h_s = ssm_scan_fwd(**g, h0=h0_d, zoh=zoh, reverse=rev)
+    y_g, h_g = ssm_scan_fwd(**dict(g, A=_misaligned_A(g["A"])), h0=h0_d, zoh=zoh, reverse=rev)
+    torch.cuda.synchronize()
+    y_ref, h_ref = oracle.ssm_scan_ref(**inp, h0=h0, zoh=zoh, reverse=rev)
+    assert rel_l2(y_s.float().cpu().numpy(), y_ref) <= TOL_Y[dt]
+    assert rel_l2(h_s.cpu().numpy(), h_ref) <= TOL_H[dt]
+    # same arithmetic, same order per state: the two kernels agree to fp32 summation order
+    assert rel_l2(h_s.cpu().numpy(), h_g.cpu().numpy()) <= 1e-6
+    assert rel_l2(y_s.float().cpu().numpy(), y_g.float().cpu().numpy()) <= (1e-6 if dt == "f32" else 1e-2)
