@@ -213,7 +213,10 @@ typedef struct ssd_scan_params {
     int64_t headdim;        /* P */
     int64_t dstate;         /* N */
     int64_t ngroups;        /* G >= 1, divides H; head h reads group h / (H / G) */
-    int64_t chunk_size;     /* Q; the result does not depend on it beyond rounding */
+    int64_t chunk_size;     /* Q >= 1, a hint: the result does not depend on it beyond rounding.
+                               The tensor-core kernel (bf16, P = 64, N = 128, 16-byte aligned
+                               tensors) always works in 128-step blocks; the CUDA-core kernel
+                               in chunks of Q. */
     int32_t io_dtype;       /* ssm_dtype_t of x, delta, B, C, z and y */
     int32_t delta_softplus; /* as for ssm_scan_params */
     const void* x;          /* (b, L, H, P) */

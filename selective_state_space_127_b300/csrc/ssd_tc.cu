@@ -637,7 +637,6 @@ bool al16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; }
 
 bool ssd_tc_supported(const SSDArgs& a) {
     if (!a.io_bf16 || a.headdim != kP || a.dstate != kN) return false;
-    if (a.chunk % kQ != 0) return false;
     if (a.nheads > 65535 || a.batch > 65535 || a.seqlen > ((int64_t)1 << 30)) return false;
     if (!al16(a.x) || !al16(a.B) || !al16(a.C) || !al16(a.y)) return false;
     if (a.z && !al16(a.z)) return false;

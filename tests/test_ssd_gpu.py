@@ -27,6 +27,15 @@ def _to(dev, inp):
     return {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
 
 
+def _misaligned_copy(t):
+    """Same values in a view whose base is off the 16-byte grid (the tensor-core kernel
+    refuses it, so the CUDA-core kernel runs)."""
+    big = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+    v = big[1:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
 CASES = [
     # b, L, H, P, N, G, Q, dtype, gate, dskip
     (1, 1, 1, 1, 1, 1, 1, "f32", False, False),
@@ -101,7 +110,7 @@ def test_tensor_core_path_matches_oracle_and_cuda_core_path(cuda_dev, b, L, H, P
     g = _to(cuda_dev, inp)
     h0_d = h0.to(cuda_dev) if h0 is not None else None
     y_tc, h_tc = ssd_chunk_scan_fwd(**g, chunk_size=Q, h0=h0_d)
-    y_cc, h_cc = ssd_chunk_scan_fwd(**g, chunk_size=64, h0=h0_d)     # not a multiple of 128: CUDA cores
+    y_cc, h_cc = ssd_chunk_scan_fwd(**dict(g, x=_misaligned_copy(g["x"])), chunk_size=64, h0=h0_d)  # CUDA cores
     torch.cuda.synchronize()
     y_ref, h_ref = oracle.ssd_scan_ref(**inp, h0=h0)
     assert rel_l2(y_tc.float().cpu().numpy(), y_ref) <= TOL_Y["bf16"]
