@@ -161,3 +161,18 @@ def test_fused_prologue_at_workload_size_sampled(cuda_dev):
     y_ref, h_ref = _fused_ref(sub, w.index_select(0, idx), cb.index_select(0, idx), None)
     assert rel_l2(y.index_select(2, idx.to(cuda_dev)).float().cpu().numpy(), y_ref) <= TOL["bf16"]
     assert rel_l2(h.index_select(1, idx.to(cuda_dev)).cpu().numpy(), h_ref) <= TOL_H["bf16"]
+
+
+def test_fused_prologue_with_exact_zoh_and_h0(cuda_dev):
+    """The conv prologue together with the exact-ZOH discretisation and an initial state (the
+    generic kernel takes this combination) against the oracle."""
+    inp, w, cb, prev = _fused_case(2, 150, 24, 16, "f32", 4, 6400, True)
+    h0 = torch.randn(2, 24, 16, generator=torch.Generator().manual_seed(64))
+    g = _to(cuda_dev, inp)
+    y, h = ssm_scan_fwd(**g, h0=h0.to(cuda_dev), zoh=True, conv_weight=w.to(cuda_dev), conv_bias=cb.to(cuda_dev),
+                        conv_x_prev=prev.to(cuda_dev))
+    torch.cuda.synchronize()
+    u = oracle.causal_conv1d_ref(inp["x"], w, cb, x_prev=prev)
+    y_ref, h_ref = oracle.ssm_scan_ref(**dict(inp, x=u), h0=h0, zoh=True)
+    assert rel_l2(y.cpu().numpy(), y_ref) <= TOL["f32"]
+    assert rel_l2(h.cpu().numpy(), h_ref) <= TOL_H["f32"]
