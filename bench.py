@@ -469,9 +469,9 @@ def run_ours(args):
     if not args.no_e2e:
         host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in inp.items()}
         bufs = {}
-        for _ in range(2):
+        for _ in range(3):
             ssm_scan_fwd_host(host, device=dev, dev_buffers=bufs, chunk_len=w.chunk_len)
-        e2e_steps = max(3, min(args.steps, 10))
+        e2e_steps = max(3, min(args.steps, 30))
         torch.cuda.synchronize()
         if barrier:
             barrier()
