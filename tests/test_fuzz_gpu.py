@@ -64,3 +64,32 @@ def test_random_configuration_matches_oracle(cuda_dev, i):
     assert rel_l2(y.float().cpu().numpy(), y_ref) <= TOL_Y[c["dt"]], c
     assert rel_l2(h.cpu().numpy(), h_ref) <= TOL_H[c["dt"]], c
     assert device_status() == binding.SSM_OK
+
+
+def _ssd_config(i):
+    r = random.Random(9500 + i)
+    P, N = r.choice([(64, 128), (64, 128), (32, 64), (16, 32), (8, 16), (64, 64)])
+    H = r.choice([1, 2, 4, 6])
+    G = r.choice([g for g in (1, 2, 3) if H % g == 0])
+    return dict(b=r.choice([1, 2]), L=r.choice([1, 7, 64, 128, 130, 300, 513]), H=H, P=P, N=N, G=G,
+                Q=r.choice([16, 64, 128, 256]), dt=r.choice(["bf16", "bf16", "f32"]), gate=r.random() < 0.4,
+                dskip=r.random() < 0.5, h0=r.random() < 0.5)
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_ssd_configuration_matches_oracle(cuda_dev, i):
+    from selective_state_space_127_b300 import ssd_chunk_scan_fwd
+    from selective_state_space_127_b300.synth import make_ssd_inputs
+    c = _ssd_config(i)
+    inp = make_ssd_inputs(c["b"], c["L"], c["H"], c["P"], c["N"], c["dt"], seed=9600 + i,
+                          d_skip="normal" if c["dskip"] else "none", gate=c["gate"], ngroups=c["G"])
+    h0 = torch.randn(c["b"], c["H"], c["N"], c["P"], generator=torch.Generator().manual_seed(9700 + i)) if c["h0"] else None
+    dev_inp = {k: (v.to(cuda_dev) if v is not None else None) for k, v in inp.items()}
+    y, h = ssd_chunk_scan_fwd(**dev_inp, chunk_size=c["Q"], h0=h0.to(cuda_dev) if h0 is not None else None)
+    torch.cuda.synchronize()
+    y_ref, h_ref = oracle.ssd_scan_ref(**inp, h0=h0)
+    # the tensor-core kernel (bf16, P = 64, N = 128) carries bf16 operands: h within 5e-3
+    tol_h = 5e-3 if c["dt"] == "bf16" else 1e-5
+    assert rel_l2(y.float().cpu().numpy(), y_ref) <= TOL_Y[c["dt"]], c
+    assert rel_l2(h.cpu().numpy(), h_ref) <= tol_h, c
+    assert device_status() == binding.SSM_OK
