@@ -9,7 +9,7 @@
  *    enqueued on it and the call returns without synchronising (except ssm_device_status).
  *  - Argument errors are detected on the host before anything is launched and return
  *    SSM_ERR_INVALID_ARG (shape, stride, pointer, dtype or alignment problem) or
- *    SSM_ERR_UNSUPPORTED (a valid request this build does not implement); a one-line
+ *    SSM_ERR_UNSUPPORTED (a valid request this library does not implement); a one-line
  *    reason is then available from ssm_last_error() on the calling thread.
  *  - A failed launch returns SSM_ERR_CUDA; the CUDA error string is in ssm_last_error().
  *  - Stateless and thread-safe: calls on different streams may run concurrently as long
