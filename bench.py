@@ -194,13 +194,14 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ oracle timing (CPU)
 
-def _oracle_sample(w, target_s):
+def _oracle_sample(w, target_s, threads=None):
     """Pick a sample (batch rows, channels) of workload w that the oracle finishes in about
-    target_s seconds on this host, from a probe of one channel per thread."""
+    target_s seconds on this host with `threads` threads (default: all), from a probe of one
+    channel per thread."""
     import oracle
     from selective_state_space_127_b300.synth import make_scan_inputs, SEED_BASE
 
-    threads = oracle.max_threads()
+    threads = threads or oracle.max_threads()
     probe_d = max(1, min(w.dim, threads))
     inp = make_scan_inputs(1, w.seqlen, probe_d, w.dstate, w.dtype, SEED_BASE + 1, "cpu", w.d_skip, w.gate)
     conv = {k: (oracle.f64(v) if v is not None else None) for k, v in inp.items()}
@@ -221,12 +222,13 @@ def _oracle_inputs(w, rows, d):
     return {k: (oracle.f64(v) if v is not None else None) for k, v in inp.items()}
 
 
-def time_oracle_scan(w, target_s=12.0):
+def time_oracle_scan(w, target_s=12.0, threads=None):
     """Time the fp64 oracle on a bounded sample of workload w (all L steps of some batch rows
-    and channels, about target_s seconds). Returns (GB/s, seconds, sample, threads)."""
+    and channels, about target_s seconds) with `threads` threads (default: all). Returns
+    (GB/s, seconds, sample, threads)."""
     import oracle
 
-    rows, d, threads = _oracle_sample(w, target_s)
+    rows, d, threads = _oracle_sample(w, target_s, threads)
     conv = _oracle_inputs(w, rows, d)
     t0 = time.perf_counter()
     oracle.ssm_scan_ref(**conv, nthreads=threads)
@@ -490,6 +492,9 @@ def run_ours(args):
         gbs, secs, sample, threads = time_oracle_scan(w)
         result["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                                   "sample": sample, "seconds": round(secs, 2)}
+        gbs1, secs1, sample1, _ = time_oracle_scan(w, 4.0, threads=1)
+        result["cpu_baseline"]["single_thread"] = {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1,
+                                                   "sample": sample1, "seconds": round(secs1, 2)}
 
     if world > 1:
         dist.barrier(device_ids=[local])
