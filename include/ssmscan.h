@@ -6,14 +6,22 @@
  *  - Pointers in the params structs are DEVICE pointers owned by the caller; the library
  *    never allocates, frees or keeps them after the call returns.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream). Work is
- *    enqueued on it and the call returns without synchronising (except ssm_device_status).
+ *    enqueued on it and the call returns without synchronising (except ssm_check_status).
  *  - Argument errors are detected on the host before anything is launched and return
  *    SSM_ERR_INVALID_ARG (shape, stride, pointer, dtype or alignment problem) or
  *    SSM_ERR_UNSUPPORTED (a valid request this library does not implement); a one-line
  *    reason is then available from ssm_last_error() on the calling thread.
  *  - A failed launch returns SSM_ERR_CUDA; the CUDA error string is in ssm_last_error().
- *  - Stateless and thread-safe: calls on different streams may run concurrently as long
- *    as their output and workspace buffers do not overlap.
+ *  - Device-side failures are reported in the caller's workspace: its first
+ *    SSM_WORKSPACE_HEADER_BYTES hold a status word that kernels with bounded waits set when a
+ *    wait gives up, and ssm_check_status() reads it. A workspace must start with that header
+ *    zeroed (cudaMemset once before its first use); ssm_check_status(..., clear = 1) zeroes it
+ *    again. Calls that need no workspace (ssm_*_workspace_size() == 0) run kernels with no
+ *    device-side waits and have nothing to report.
+ *  - Thread-safe. Calls on different streams may run concurrently as long as their output and
+ *    workspace buffers do not overlap. The library keeps no state between calls besides the
+ *    calling thread's last-error string, a process-wide count of launched kernels, and the
+ *    fixed scratch buffer of ssm_scan_fwd_noalloc (see there).
  *  - Arithmetic: inputs in the I/O dtype (fp32 or bf16) are widened to fp32; the state and
  *    every intermediate are fp32; y is rounded to the I/O dtype (round to nearest even).
  *
@@ -30,7 +38,11 @@
 extern "C" {
 #endif
 
-#define SSMSCAN_ABI_VERSION 2
+#define SSMSCAN_ABI_VERSION 3
+
+/* Bytes at the start of every workspace that hold the device status word (a uint32 at offset 0;
+ * the rest is reserved). */
+#define SSM_WORKSPACE_HEADER_BYTES 256
 
 #if defined(__GNUC__)
 #define SSMSCAN_API __attribute__((visibility("default")))
@@ -43,7 +55,7 @@ typedef enum {
     SSM_ERR_INVALID_ARG = 1,
     SSM_ERR_UNSUPPORTED = 2,
     SSM_ERR_CUDA = 3,
-    SSM_ERR_TIMEOUT = 4,   /* a bounded device-side wait gave up (see ssm_device_status) */
+    SSM_ERR_TIMEOUT = 4,   /* a bounded device-side wait gave up (see ssm_check_status) */
     SSM_ERR_WORKSPACE = 5  /* workspace missing, too small or misaligned */
 } ssm_status_t;
 
@@ -60,7 +72,7 @@ typedef enum { SSM_DISC_DELTA_B = 0, SSM_DISC_ZOH = 1 } ssm_discretization_t;
 
 /* Test hooks (debug_flags). SSM_DEBUG_SKIP_FIRST_LOAD: the TMA path never issues the copy
  * of its first tile, so its bounded wait runs out (about one second), the kernel latches
- * SSM_ERR_TIMEOUT in the device status word and returns with nothing in flight. Accepted
+ * SSM_ERR_TIMEOUT in the workspace's status word and returns with nothing in flight. Accepted
  * only when the whole sequence fits in that first tile (5 <= L <= 16) and the TMA path
  * applies; otherwise the call returns SSM_ERR_INVALID_ARG. */
 #define SSM_DEBUG_SKIP_FIRST_LOAD 1
@@ -74,9 +86,9 @@ typedef enum { SSM_DISC_DELTA_B = 0, SSM_DISC_ZOH = 1 } ssm_discretization_t;
  *   y     *= silu(z[b,t,d]) = z / (1 + e^-z)
  * The output at t reads the state after x_t has entered it. The state starts at h0
  * (zeros when NULL) and its value after the last step is written to h_last. h_last may be
- * the same buffer as h0: with L = 1 that is the single-token (decode) step that advances a
- * cached state in place ("Mamba/SSM complete guide" section 2: recurrent inference with a
- * constant-size state).
+ * the same buffer as h0 (any L, any chunking: the state is read before it is overwritten);
+ * with L = 1 that is the single-token (decode) step that advances a cached state in place
+ * ("Mamba/SSM complete guide" section 2: recurrent inference with a constant-size state).
  * Pages: "Mamba/SSM complete guide" section 5, listing `selective_scan` (discretise, loop,
  * readout, u*D) and MambaBlock.forward (y * silu(z)); "論文解説: Mamba" "選択機構"
  * (softplus) and "Hardware-Aware Parallel Scan" (the recurrence, zero initial state).
@@ -105,7 +117,8 @@ typedef struct ssm_scan_params {
     const float* D;         /* (D) fp32 or NULL (no skip) */
     const float* delta_bias;/* (D) fp32 or NULL (zero bias) */
     const float* h0;        /* (b, D, N) fp32 contiguous, or NULL (zeros) */
-    void* y;                /* (b, L, D) in io_dtype, strides y_stride; must not alias inputs */
+    void* y;                /* (b, L, D) in io_dtype, strides y_stride; its memory range must not
+                               overlap that of any input (checked) */
     float* h_last;          /* (b, D, N) fp32 contiguous, or NULL (not written) */
     int64_t x_stride[3];    /* element strides for (b, t, d); 0 broadcasts */
     int64_t delta_stride[3];
@@ -118,9 +131,11 @@ typedef struct ssm_scan_params {
                                >= L, the reverse direction, or a path that does not split: one
                                chunk); 0 = let the library choose. The result does not depend on
                                it beyond fp32 rounding. With more than one chunk the call needs
-                               (nchunks - 1) * b * D * (N + 1) * 4 bytes of workspace. */
+                               nchunks * b * D * N * 4 + (nchunks - 1) * b * D * 4 bytes of
+                               workspace after the header. */
     void* workspace;        /* device scratch of ssm_scan_workspace_size() bytes, 256-byte
-                               aligned; may be NULL when that size is 0 */
+                               aligned, header zeroed before first use (see above); may be NULL
+                               when that size is 0 */
     size_t workspace_bytes;
     int32_t debug_flags;    /* 0 in normal use; SSM_DEBUG_* test hooks */
     int32_t reserved;       /* must be 0 */
@@ -130,10 +145,21 @@ typedef struct ssm_scan_params {
                                  x[:, 0] (the tail of the previous segment), or NULL (zeros) */
     int32_t conv_width;       /* K, 1 <= K <= 4, when conv_weight is set; ignored otherwise */
     int32_t reserved2;        /* must be 0 */
+    void* const* phase_events;/* NULL, or n_phase_events cudaEvent_t handles (passed as void*) for
+                                 timing the call's kernels: events[0] is recorded on the stream
+                                 before the first kernel the call launches and events[k] after its
+                                 k-th kernel; entries past the last kernel are recorded after it
+                                 too (the long-sequence path launches 3 kernels: local pass, chunk
+                                 carry, output pass; the others 1) */
+    int32_t n_phase_events;   /* entries of phase_events (0 when it is NULL) */
+    int32_t reserved3;        /* must be 0 */
 } ssm_scan_params;
 
-/* Bytes of device workspace ssm_scan_fwd needs for these params (0 if none). Host only,
- * no CUDA call. Returns (size_t)-1 when the params are invalid. */
+/* Bytes of device workspace ssm_scan_fwd needs for these params: 0 for the paths without
+ * device-side waits (short sequences, generic layouts), else SSM_WORKSPACE_HEADER_BYTES plus
+ * the chunk carries of a split sequence. Host only; its first call may look up a driver entry
+ * point (cudaGetDriverEntryPointByVersion), nothing else. Returns (size_t)-1 when the params
+ * are invalid. */
 SSMSCAN_API size_t ssm_scan_workspace_size(const ssm_scan_params* p);
 
 /* Enqueue the selective scan on `stream`. Returns SSM_OK once launched. */
@@ -146,21 +172,26 @@ SSMSCAN_API ssm_status_t ssm_scan_fwd(const ssm_scan_params* p, void* stream);
  * device allocations), and callers that cannot afford cudaMalloc's implicit synchronisation.
  *  - Same arguments and results as ssm_scan_fwd; p->workspace and p->workspace_bytes are
  *    ignored. Inputs and outputs are still the caller's.
- *  - The scratch of the chunked (long-sequence) path comes from a buffer compiled into the
- *    library, SSM_NOALLOC_SCRATCH_BYTES (16 MiB) of device memory on every GPU that loads the
- *    library, held until the process exits. A call that needs more
+ *  - The workspace (status header and the chunk carries of the long-sequence path) comes from
+ *    a buffer compiled into the library, SSM_NOALLOC_SCRATCH_BYTES (16 MiB) of device memory
+ *    on every GPU that loads the library, held until the process exits (the same value is
+ *    returned by ssm_noalloc_scratch_bytes()). A call that needs more
  *    (ssm_scan_workspace_size(p) > SSM_NOALLOC_SCRATCH_BYTES) returns SSM_ERR_UNSUPPORTED
  *    before anything is launched; a larger chunk_len needs less.
  *  - The first call on a device looks up the buffer's device address (cudaGetSymbolAddress)
  *    with that device current; make that first call before any stream capture.
- *  - Every call shares the one buffer, which keeps the last call's contents (nothing in it has
- *    to start at zero: each call writes every element it later reads). Calls whose work
- *    overlaps on the GPU (different streams, or different host threads) race on it: serialise
- *    them.
+ *  - Every call shares the one buffer, which keeps the last call's contents (the carries need
+ *    no zeroing: each call writes every element it later reads; the status header starts at
+ *    zero when the library loads and is read and cleared by ssm_check_status(NULL, ...)).
+ *    Calls whose work overlaps on the GPU (different streams, or different host threads) race
+ *    on it: serialise them.
  *  - It calls no cudaMalloc, cudaFree or other allocating routine.
  */
 #define SSM_NOALLOC_SCRATCH_BYTES (16u << 20)
 SSMSCAN_API ssm_status_t ssm_scan_fwd_noalloc(const ssm_scan_params* p, void* stream);
+
+/* SSM_NOALLOC_SCRATCH_BYTES of the library that was loaded. */
+SSMSCAN_API size_t ssm_noalloc_scratch_bytes(void);
 
 /*
  * Causal depthwise convolution along t with K taps per channel, then optionally SiLU: the
@@ -187,7 +218,15 @@ typedef struct ssm_conv1d_params {
     const float* bias;      /* (D) fp32 or NULL */
     const void* x_prev;     /* (b, K-1, D) or NULL (zeros) */
     void* y;                /* (b, L, D); must not overlap x or x_prev */
+    void* workspace;        /* SSM_WORKSPACE_HEADER_BYTES of device memory (the status word of its
+                               bounded waits), 256-byte aligned, header zeroed before first use;
+                               may be NULL when L == 0 */
+    size_t workspace_bytes;
 } ssm_conv1d_params;
+
+/* Bytes of device workspace ssm_causal_conv1d_fwd needs (SSM_WORKSPACE_HEADER_BYTES, or 0
+ * when L == 0); (size_t)-1 if the params are invalid. */
+SSMSCAN_API size_t ssm_causal_conv1d_workspace_size(const ssm_conv1d_params* p);
 
 /* Enqueue the convolution on `stream`. Returns SSM_OK once launched. */
 SSMSCAN_API ssm_status_t ssm_causal_conv1d_fwd(const ssm_conv1d_params* p, void* stream);
@@ -230,22 +269,27 @@ typedef struct ssd_scan_params {
     const float* h0;        /* (b, H, N, P) fp32 or NULL */
     void* y;                /* (b, L, H, P) in io_dtype */
     float* h_last;          /* (b, H, N, P) fp32 or NULL */
-    void* workspace;        /* device scratch, 256-byte aligned */
+    void* workspace;        /* device scratch of ssd_chunk_scan_workspace_size() bytes, 256-byte
+                               aligned, header zeroed before first use; may be NULL when that
+                               size is 0 */
     size_t workspace_bytes;
 } ssd_scan_params;
 
-/* Bytes of device workspace ssd_chunk_scan_fwd needs (0 if none); (size_t)-1 if invalid. */
+/* Bytes of device workspace ssd_chunk_scan_fwd needs: SSM_WORKSPACE_HEADER_BYTES on the
+ * tensor-core path (its bounded waits), 0 on the CUDA-core path; (size_t)-1 if invalid. */
 SSMSCAN_API size_t ssd_chunk_scan_workspace_size(const ssd_scan_params* p);
 
 /* Enqueue the SSD chunked scan on `stream`. Returns SSM_OK once launched. */
 SSMSCAN_API ssm_status_t ssd_chunk_scan_fwd(const ssd_scan_params* p, void* stream);
 
-/* Synchronise `stream`, then return the library's device status word for the current
- * device: SSM_OK, or SSM_ERR_TIMEOUT if a kernel's bounded wait on its own TMA copies gave up
- * since the word was last cleared (that kernel's outputs are then incomplete). With
- * `clear` != 0 the word is reset to SSM_OK afterwards. Returns SSM_ERR_CUDA if the stream
- * reports an error. */
-SSMSCAN_API ssm_status_t ssm_device_status(void* stream, int clear);
+/* Synchronise `stream`, then return the status word in the header of `workspace` (a device
+ * pointer given to earlier calls on this stream): SSM_OK, or SSM_ERR_TIMEOUT if a bounded
+ * wait of a kernel that used this workspace gave up since the word was last cleared (that
+ * call's outputs are then incomplete). A timeout is visible only through the workspace of
+ * the call that had it. workspace == NULL reads the header of the built-in scratch of
+ * ssm_scan_fwd_noalloc on the current device. With `clear` != 0 the word is reset to SSM_OK
+ * afterwards. Returns SSM_ERR_CUDA if the stream reports an error. */
+SSMSCAN_API ssm_status_t ssm_check_status(void* workspace, void* stream, int clear);
 
 /* Static, human-readable name of a status code. */
 SSMSCAN_API const char* ssm_status_string(ssm_status_t s);

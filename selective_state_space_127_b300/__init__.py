@@ -3,8 +3,8 @@
 The compute lives in libssmscan.so (CUDA for sm_103a, C ABI in include/ssmscan.h); this
 package holds its build script, a ctypes binding and the seeded input generators.
 """
-from .binding import (SSMError, causal_conv1d_fwd, load_library, ssd_chunk_scan_fwd, ssm_scan_fwd,
-                      ssm_scan_fwd_host, device_status)
+from .binding import (SSMError, ScanCall, causal_conv1d_fwd, check_status, load_library, new_workspace,
+                      ssd_chunk_scan_fwd, ssm_scan_fwd, ssm_scan_fwd_host)
 
-__all__ = ["SSMError", "load_library", "ssm_scan_fwd", "ssd_chunk_scan_fwd", "ssm_scan_fwd_host",
-           "causal_conv1d_fwd", "device_status"]
+__all__ = ["SSMError", "ScanCall", "load_library", "ssm_scan_fwd", "ssd_chunk_scan_fwd", "ssm_scan_fwd_host",
+           "causal_conv1d_fwd", "check_status", "new_workspace"]

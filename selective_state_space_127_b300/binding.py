@@ -20,13 +20,14 @@ LIB_PATH = os.path.join(_PKG, "libssmscan.so")
 SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_WORKSPACE = range(6)
 SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
 SSM_DISC_DELTA_B, SSM_DISC_ZOH = 0, 1
-ABI_VERSION = 2
+ABI_VERSION = 3
+WORKSPACE_HEADER_BYTES = 256   # SSM_WORKSPACE_HEADER_BYTES: the status word of a workspace
 
 # Every function the header declares (checked by the CPU test suite).
 EXPORTS = ("ssm_scan_workspace_size", "ssm_scan_fwd", "ssd_chunk_scan_workspace_size", "ssd_chunk_scan_fwd",
-           "ssm_device_status", "ssm_status_string", "ssm_last_error", "ssm_abi_version",
-           "ssm_kernel_launch_count", "ssm_scan_fwd_noalloc", "ssm_causal_conv1d_fwd")
-NOALLOC_SCRATCH_BYTES = 16 << 20
+           "ssm_check_status", "ssm_status_string", "ssm_last_error", "ssm_abi_version",
+           "ssm_kernel_launch_count", "ssm_scan_fwd_noalloc", "ssm_noalloc_scratch_bytes",
+           "ssm_causal_conv1d_workspace_size", "ssm_causal_conv1d_fwd")
 
 _i64, _i32, _vp, _sz = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t
 
@@ -41,13 +42,14 @@ class ScanParams(ctypes.Structure):
                 ("chunk_len", _i64), ("workspace", _vp), ("workspace_bytes", _sz),
                 ("debug_flags", _i32), ("reserved", _i32),
                 ("conv_weight", _vp), ("conv_bias", _vp), ("conv_x_prev", _vp), ("conv_width", _i32),
-                ("reserved2", _i32)]
+                ("reserved2", _i32), ("phase_events", ctypes.POINTER(_vp)), ("n_phase_events", _i32),
+                ("reserved3", _i32)]
 
 
 class Conv1dParams(ctypes.Structure):
     _fields_ = [("batch", _i64), ("seqlen", _i64), ("dim", _i64), ("width", _i32), ("io_dtype", _i32),
                 ("silu", _i32), ("reserved", _i32), ("x", _vp), ("weight", _vp), ("bias", _vp),
-                ("x_prev", _vp), ("y", _vp)]
+                ("x_prev", _vp), ("y", _vp), ("workspace", _vp), ("workspace_bytes", _sz)]
 
 SSM_DEBUG_SKIP_FIRST_LOAD = 1
 
@@ -87,8 +89,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.ssd_chunk_scan_workspace_size.restype = _sz
             lib.ssd_chunk_scan_fwd.argtypes = [ctypes.POINTER(SSDParams), _vp]
             lib.ssd_chunk_scan_fwd.restype = ctypes.c_int
-            lib.ssm_device_status.argtypes = [_vp, ctypes.c_int]
-            lib.ssm_device_status.restype = ctypes.c_int
+            lib.ssm_check_status.argtypes = [_vp, _vp, ctypes.c_int]
+            lib.ssm_check_status.restype = ctypes.c_int
+            lib.ssm_noalloc_scratch_bytes.argtypes = []
+            lib.ssm_noalloc_scratch_bytes.restype = _sz
+            lib.ssm_causal_conv1d_workspace_size.argtypes = [ctypes.POINTER(Conv1dParams)]
+            lib.ssm_causal_conv1d_workspace_size.restype = _sz
             lib.ssm_status_string.argtypes = [ctypes.c_int]
             lib.ssm_status_string.restype = ctypes.c_char_p
             lib.ssm_last_error.argtypes = []
@@ -150,9 +156,35 @@ def _stream_handle(stream) -> int:
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A device workspace of ``nbytes`` (at least the status header) with its header zeroed, as
+    the library expects before a workspace's first use. PyTorch's allocator returns blocks
+    aligned to at least 256 bytes."""
+    return torch.zeros(max(int(nbytes), WORKSPACE_HEADER_BYTES), dtype=torch.uint8, device=device)
+
+
+def noalloc_scratch_bytes() -> int:
+    """Size of the built-in scratch of ssm_scan_fwd_noalloc, as compiled into the library."""
+    return int(load_library().ssm_noalloc_scratch_bytes())
+
+
+def _event_array(events):
+    """ctypes array of cudaEvent_t handles of torch.cuda.Event objects (each created by a
+    record on the current stream first, since torch creates events lazily)."""
+    if not events:
+        return None, 0
+    handles = []
+    for ev in events:
+        if ev.cuda_event == 0:
+            ev.record()
+        handles.append(ev.cuda_event)
+    arr = (_vp * len(handles))(*handles)
+    return arr, len(handles)
+
+
 def _scan_params(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_softplus=True, h0=None,
                  reverse=False, zoh=False, chunk_len=0, out=None, return_last_state=True, h_last=None,
-                 debug_flags=0, conv_weight=None, conv_bias=None, conv_x_prev=None):
+                 debug_flags=0, conv_weight=None, conv_bias=None, conv_x_prev=None, phase_events=None):
     """Check the tensors and fill a ScanParams; returns (params, y, h_last)."""
     if not x.is_cuda:
         raise ValueError("x must be a CUDA tensor (use ssm_scan_fwd_host for host buffers)")
@@ -204,6 +236,10 @@ def _scan_params(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_so
     if conv_weight is not None:
         p.conv_weight, p.conv_bias, p.conv_x_prev = _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_x_prev)
         p.conv_width = K
+    arr, n = _event_array(phase_events)
+    if arr is not None:
+        p.phase_events, p.n_phase_events = ctypes.cast(arr, ctypes.POINTER(_vp)), n
+        p._events_keepalive = arr
     return p, y, hl
 
 
@@ -220,37 +256,80 @@ def scan_workspace_size(x, delta, A, B, C, D=None, z=None, delta_bias=None, **kw
 
 def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_softplus=True, h0=None,
                  reverse=False, zoh=False, chunk_len=0, out=None, return_last_state=True, h_last=None,
-                 stream=None, workspace=None, debug_flags=0, conv_weight=None, conv_bias=None, conv_x_prev=None):
+                 stream=None, workspace=None, debug_flags=0, conv_weight=None, conv_bias=None, conv_x_prev=None,
+                 phase_events=None):
     """Selective scan on the GPU. x, delta, z: (b, L, D); B, C: (b, L, N); A: (D, N) fp32;
     D, delta_bias: (D) fp32; h0: (b, D, N) fp32. I/O tensors are fp32 or bf16 (all alike) and
     may be strided (delta's channel stride may be 0). ``workspace`` (a uint8 CUDA tensor of at
-    least scan_workspace_size() bytes, 256-byte aligned) is allocated when not given.
+    least scan_workspace_size() bytes, 256-byte aligned, its first 256 bytes zeroed before
+    first use, e.g. from new_workspace()) holds the status word read by check_status() and the
+    chunk carries of long sequences; a fresh one is allocated when not given (or too small).
     With ``conv_weight`` (D, K) fp32 (K <= 4), x is the raw input and the scan runs on
     silu(causal conv1d(x) + conv_bias); ``conv_x_prev`` (b, K-1, D) holds the K-1 raw inputs
-    before x[:, 0] (zeros when None). Returns (y, h_last or None)."""
+    before x[:, 0] (zeros when None). ``phase_events``: torch.cuda.Event objects recorded
+    before the call's first kernel and after each kernel. Returns (y, h_last or None)."""
     lib = load_library()
     p, y, hl = _scan_params(x, delta, A, B, C, D, z, delta_bias, delta_softplus=delta_softplus, h0=h0,
                             reverse=reverse, zoh=zoh, chunk_len=chunk_len, out=out,
                             return_last_state=return_last_state, h_last=h_last, debug_flags=debug_flags,
-                            conv_weight=conv_weight, conv_bias=conv_bias, conv_x_prev=conv_x_prev)
+                            conv_weight=conv_weight, conv_bias=conv_bias, conv_x_prev=conv_x_prev,
+                            phase_events=phase_events)
     ws_bytes = lib.ssm_scan_workspace_size(ctypes.byref(p))
     if ws_bytes == ctypes.c_size_t(-1).value:
         _check(lib, lib.ssm_scan_fwd(ctypes.byref(p), None))  # raises with the reason
     if ws_bytes > 0:
         ws = workspace
         if ws is None or ws.numel() < ws_bytes:
-            ws = torch.empty(ws_bytes, device=x.device, dtype=torch.uint8)
+            ws = new_workspace(ws_bytes, x.device)
         p.workspace, p.workspace_bytes = _ptr(ws), ws.numel()
     with torch.cuda.device(x.device):
         _check(lib, lib.ssm_scan_fwd(ctypes.byref(p), _stream_handle(stream)))
     return y, hl
 
 
+class ScanCall:
+    """A prepared selective-scan call for repeated use on the same buffers (a decode loop, a
+    benchmark): the arguments of ssm_scan_fwd are checked and the C params struct is filled
+    once, with the outputs and the workspace bound; each call then only enqueues the C call on
+    the stream. Returns (y, h_last) like ssm_scan_fwd."""
+
+    def __init__(self, x, delta, A, B, C, D=None, z=None, delta_bias=None, *, out=None, h_last=None,
+                 workspace=None, stream=None, **kw):
+        self._lib = load_library()
+        p, self.y, self.h_last = _scan_params(x, delta, A, B, C, D, z, delta_bias, out=out, h_last=h_last, **kw)
+        n = self._lib.ssm_scan_workspace_size(ctypes.byref(p))
+        if n == ctypes.c_size_t(-1).value:
+            _check(self._lib, self._lib.ssm_scan_fwd(ctypes.byref(p), None))
+        self.workspace = workspace if workspace is not None and workspace.numel() >= n else \
+            (new_workspace(n, x.device) if n > 0 else None)
+        if self.workspace is not None:
+            p.workspace, p.workspace_bytes = _ptr(self.workspace), self.workspace.numel()
+        self._p = p
+        self._ref = ctypes.byref(p)
+        self._device = x.device
+        self._keep = (x, delta, A, B, C, D, z, delta_bias, kw.get("h0"), kw.get("conv_weight"),
+                      kw.get("conv_bias"), kw.get("conv_x_prev"))
+        self._stream = _stream_handle(stream) if stream is not None else None
+
+    def __call__(self, stream=None):
+        if stream is not None:
+            sh = _stream_handle(stream)
+        elif self._stream is not None:
+            sh = self._stream
+        else:
+            sh = ctypes.c_void_p(torch.cuda.current_stream(self._device).cuda_stream)
+        s = self._lib.ssm_scan_fwd(self._ref, sh)
+        if s != SSM_OK:
+            _check(self._lib, s)
+        return self.y, self.h_last
+
+
 def ssm_scan_fwd_noalloc(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_softplus=True, h0=None,
                          chunk_len=0, out=None, return_last_state=True, h_last=None, stream=None):
     """The allocation-free C entry point (no workspace: the library's built-in scratch is
-    used). Outputs are allocated here when not given; pass ``out`` and ``h_last`` to keep the
-    call itself free of allocations. Returns (y, h_last or None)."""
+    used; its status word is read by check_status(None)). Outputs are allocated here when not
+    given; pass ``out`` and ``h_last`` to keep the call itself free of allocations. Returns
+    (y, h_last or None)."""
     lib = load_library()
     p, y, hl = _scan_params(x, delta, A, B, C, D, z, delta_bias, delta_softplus=delta_softplus, h0=h0,
                             chunk_len=chunk_len, out=out, return_last_state=return_last_state, h_last=h_last)
@@ -259,7 +338,7 @@ def ssm_scan_fwd_noalloc(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, 
     return y, hl
 
 
-def causal_conv1d_fwd(x, weight, bias=None, *, silu=True, x_prev=None, out=None, stream=None):
+def causal_conv1d_fwd(x, weight, bias=None, *, silu=True, x_prev=None, out=None, stream=None, workspace=None):
     """Causal depthwise conv1d along t (then SiLU when ``silu``) on the GPU. x: (b, L, D)
     contiguous fp32 or bf16 with D * element size a multiple of 16 bytes; weight: (D, K) fp32
     (K <= 4; weight[:, K-1] multiplies x_t); bias: (D) fp32; x_prev: (b, K-1, D) like x, the
@@ -282,6 +361,12 @@ def causal_conv1d_fwd(x, weight, bias=None, *, silu=True, x_prev=None, out=None,
     p.batch, p.seqlen, p.dim, p.width = b, L, Dm, K
     p.io_dtype, p.silu = _io_dtype(x), int(bool(silu))
     p.x, p.weight, p.bias, p.x_prev, p.y = _ptr(x), _ptr(weight), _ptr(bias), _ptr(x_prev), _ptr(y)
+    ws_bytes = lib.ssm_causal_conv1d_workspace_size(ctypes.byref(p))
+    if ws_bytes == ctypes.c_size_t(-1).value:
+        _check(lib, lib.ssm_causal_conv1d_fwd(ctypes.byref(p), None))
+    if ws_bytes > 0:
+        ws = workspace if workspace is not None and workspace.numel() >= ws_bytes else new_workspace(ws_bytes, dev)
+        p.workspace, p.workspace_bytes = _ptr(ws), ws.numel()
     with torch.cuda.device(dev):
         _check(lib, lib.ssm_causal_conv1d_fwd(ctypes.byref(p), _stream_handle(stream)))
     return y
@@ -289,7 +374,7 @@ def causal_conv1d_fwd(x, weight, bias=None, *, silu=True, x_prev=None, out=None,
 
 def ssd_chunk_scan_fwd(x, delta, A, B, C, chunk_size=256, D=None, z=None, delta_bias=None, *,
                        delta_softplus=True, h0=None, out=None, return_last_state=True, h_last=None,
-                       stream=None):
+                       stream=None, workspace=None):
     """SSD chunked scan on the GPU. x, z: (b, L, H, P); delta: (b, L, H); A, D, delta_bias: (H)
     fp32; B, C: (b, L, G, N) or (b, L, N); h0: (b, H, N, P) fp32. Contiguous tensors only.
     Returns (y, h_last or None)."""
@@ -325,10 +410,9 @@ def ssd_chunk_scan_fwd(x, delta, A, B, C, chunk_size=256, D=None, z=None, delta_
     ws_bytes = lib.ssd_chunk_scan_workspace_size(ctypes.byref(p))
     if ws_bytes == ctypes.c_size_t(-1).value:
         _check(lib, lib.ssd_chunk_scan_fwd(ctypes.byref(p), None))
-    ws = None
     if ws_bytes > 0:
-        ws = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
-        p.workspace, p.workspace_bytes = _ptr(ws), ws_bytes
+        ws = workspace if workspace is not None and workspace.numel() >= ws_bytes else new_workspace(ws_bytes, dev)
+        p.workspace, p.workspace_bytes = _ptr(ws), ws.numel()
     with torch.cuda.device(dev):
         _check(lib, lib.ssd_chunk_scan_fwd(ctypes.byref(p), _stream_handle(stream)))
     return y, hl
@@ -395,7 +479,7 @@ def ssm_scan_fwd_host(inputs: dict, device="cuda", stream=None, dev_buffers: dic
         ws = cache.get("_workspace")
         if need > 0 and (ws is None or ws.numel() < need):
             with torch.cuda.stream(s_comp):
-                ws = torch.empty(need, dtype=torch.uint8, device=dev)
+                ws = new_workspace(need, dev)
             cache["_workspace"] = ws
         ssm_scan_fwd(**sl, h0=h0, out=y_dev[r0:r1], h_last=hl_dev[r0:r1], stream=s_comp,
                      workspace=ws if need > 0 else None, **ckw)
@@ -412,8 +496,10 @@ def kernel_launch_count() -> int:
     return int(load_library().ssm_kernel_launch_count())
 
 
-def device_status(clear: bool = True, stream=None) -> int:
-    """Synchronise the stream and return the library's device status word (SSM_OK or
-    SSM_ERR_TIMEOUT), clearing it by default."""
+def check_status(workspace, clear: bool = True, stream=None) -> int:
+    """Synchronise the stream and return the status word of ``workspace`` (the uint8 tensor
+    given to earlier calls; None = the built-in scratch of ssm_scan_fwd_noalloc): SSM_OK or
+    SSM_ERR_TIMEOUT. Clears it by default."""
     lib = load_library()
-    return lib.ssm_device_status(_stream_handle(stream), int(bool(clear)))
+    ptr = None if workspace is None else ctypes.c_void_p(workspace.data_ptr())
+    return lib.ssm_check_status(ptr, _stream_handle(stream), int(bool(clear)))

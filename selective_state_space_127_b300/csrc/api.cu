@@ -67,7 +67,36 @@ bool non_overlapping(const int64_t* sizes, const int64_t* st, int nd) {
     return true;
 }
 
+// Byte range [lo, hi) spanned by a strided view with non-negative strides (empty if any size is 0).
+struct Span {
+    uintptr_t lo = 0, hi = 0;
+};
+
+Span span_of(const void* p, const int64_t* sizes, const int64_t* st, int nd, size_t esz) {
+    Span r;
+    if (!p) return r;
+    int64_t ext = 0;
+    for (int i = 0; i < nd; ++i) {
+        if (sizes[i] <= 0) return r;
+        ext += (sizes[i] - 1) * st[i];
+    }
+    r.lo = reinterpret_cast<uintptr_t>(p);
+    r.hi = r.lo + (uintptr_t)(ext * (int64_t)esz + (int64_t)esz);
+    return r;
+}
+
+Span span_dense(const void* p, int64_t elems, size_t esz) {
+    Span r;
+    if (!p || elems <= 0) return r;
+    r.lo = reinterpret_cast<uintptr_t>(p);
+    r.hi = r.lo + (uintptr_t)elems * esz;
+    return r;
+}
+
+bool overlap(const Span& a, const Span& b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
+
 constexpr int64_t kMaxDState = 256;
+constexpr int kMaxPhaseEvents = 64;
 constexpr int kMaxConvWidth = 4;
 
 ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
@@ -85,8 +114,12 @@ ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
     if ((p->delta_softplus != 0 && p->delta_softplus != 1) || (p->reverse != 0 && p->reverse != 1))
         return fail(SSM_ERR_INVALID_ARG, "delta_softplus and reverse must be 0 or 1");
     if (p->chunk_len < 0) return fail(SSM_ERR_INVALID_ARG, "chunk_len must be >= 0");
-    if (p->reserved != 0 || p->reserved2 != 0 || (p->debug_flags & ~SSM_DEBUG_SKIP_FIRST_LOAD) != 0)
+    if (p->reserved != 0 || p->reserved2 != 0 || p->reserved3 != 0 ||
+        (p->debug_flags & ~SSM_DEBUG_SKIP_FIRST_LOAD) != 0)
         return fail(SSM_ERR_INVALID_ARG, "unknown debug_flags or nonzero reserved field");
+    if (p->n_phase_events < 0 || p->n_phase_events > kMaxPhaseEvents || (p->n_phase_events > 0) != (p->phase_events != nullptr))
+        return fail(SSM_ERR_INVALID_ARG, "phase_events must be NULL with n_phase_events == 0, or hold 1..%d events",
+                    kMaxPhaseEvents);
     if (!p->A) return fail(SSM_ERR_INVALID_ARG, "A is NULL");
     if (p->conv_weight) {
         if (p->conv_width < 1 || p->conv_width > kMaxConvWidth)
@@ -110,11 +143,34 @@ ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
     const int64_t ysz[3] = {p->batch, p->seqlen, p->dim};
     if (p->seqlen > 0 && !non_overlapping(ysz, p->y_stride, 3))
         return fail(SSM_ERR_INVALID_ARG, "y strides overlap");
-    if (p->h_last && p->h0 && p->h_last != p->h0) {
-        const char* a0 = reinterpret_cast<const char*>(p->h0);
-        const char* a1 = reinterpret_cast<const char*>(p->h_last);
-        const int64_t bytes = p->batch * p->dim * p->dstate * 4;
-        if (a1 < a0 + bytes && a0 < a1 + bytes) return fail(SSM_ERR_INVALID_ARG, "h0 and h_last partly overlap");
+    const int64_t state_elems = p->batch * p->dim * p->dstate;
+    if (p->h_last && p->h0 && p->h_last != p->h0 &&
+        overlap(span_dense(p->h0, state_elems, 4), span_dense(p->h_last, state_elems, 4)))
+        return fail(SSM_ERR_INVALID_ARG, "h0 and h_last partly overlap");
+    if (p->seqlen > 0) {
+        // y and h_last are written while every input is still being read: their memory may
+        // not overlap any input (h_last may be h0 itself, which is read before it is written)
+        const int64_t act[3] = {p->batch, p->seqlen, p->dim};
+        const int64_t bc[3] = {p->batch, p->seqlen, p->dstate};
+        const Span ys = span_of(p->y, act, p->y_stride, 3, esz);
+        const Span hs = span_dense(p->h_last, state_elems, 4);
+        const int K = p->conv_weight ? p->conv_width : 0;
+        const Span ins[] = {span_of(p->x, act, p->x_stride, 3, esz),
+                            span_of(p->delta, act, p->delta_stride, 3, esz),
+                            span_of(p->z, act, p->z_stride, 3, esz),
+                            span_of(p->B, bc, p->B_stride, 3, esz),
+                            span_of(p->C, bc, p->C_stride, 3, esz),
+                            span_dense(p->A, p->dim * p->dstate, 4),
+                            span_dense(p->D, p->dim, 4),
+                            span_dense(p->delta_bias, p->dim, 4),
+                            span_dense(p->h0 != p->h_last ? p->h0 : nullptr, state_elems, 4),
+                            span_dense(p->conv_weight, p->dim * K, 4),
+                            span_dense(p->conv_weight ? p->conv_bias : nullptr, p->dim, 4),
+                            span_dense(p->conv_weight ? p->conv_x_prev : nullptr, p->batch * (K - 1) * p->dim, esz)};
+        for (const Span& in : ins)
+            if (overlap(ys, in) || overlap(hs, in))
+                return fail(SSM_ERR_INVALID_ARG, "y or h_last overlaps an input");
+        if (overlap(ys, hs)) return fail(SSM_ERR_INVALID_ARG, "y and h_last overlap");
     }
     ssm::ScanArgs& a = *out;
     a.batch = p->batch;
@@ -152,6 +208,9 @@ ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
     a.conv_b = p->conv_weight ? p->conv_bias : nullptr;
     a.conv_prev = p->conv_weight ? p->conv_x_prev : nullptr;
     a.conv_k = p->conv_weight ? p->conv_width : 0;
+    a.status = nullptr;
+    a.phase_events = p->phase_events;
+    a.n_phase_events = p->n_phase_events;
     return SSM_OK;
 }
 
@@ -197,6 +256,7 @@ ssm_status_t validate_conv1d(const ssm_conv1d_params* p, ssm::Conv1dArgs* out) {
     a.bias = p->bias;
     a.x_prev = p->x_prev;
     a.y = p->y;
+    a.status = nullptr;
     return SSM_OK;
 }
 
@@ -205,8 +265,11 @@ ssm_status_t validate_conv1d(const ssm_conv1d_params* p, ssm::Conv1dArgs* out) {
 // written once (in place when h0 == h_last).
 constexpr int64_t kShortSeq = 4;
 
+// The TMA kernels wait (bounded) on their copies, so they need the status header; the split
+// sequence adds its chunk carries after it. The short-sequence and generic kernels need none.
 size_t scan_workspace_bytes(const ssm::ScanArgs& a) {
-    return a.seqlen > kShortSeq && ssm::scan_fast_supported(a) ? ssm::scan_fast_workspace_bytes(a) : 0;
+    if (a.seqlen <= kShortSeq || !ssm::scan_fast_supported(a)) return 0;
+    return SSM_WORKSPACE_HEADER_BYTES + ssm::scan_fast_workspace_bytes(a);
 }
 
 ssm_status_t cuda_fail(cudaError_t e) {
@@ -262,6 +325,15 @@ ssm_status_t validate_ssd(const ssd_scan_params* p, ssm::SSDArgs* out) {
     a.h_last = p->h_last;
     a.workspace = p->workspace;
     a.workspace_bytes = p->workspace_bytes;
+    a.status = nullptr;
+    return SSM_OK;
+}
+
+// Check a workspace of `need` bytes (need > 0) and point `status` at its header.
+ssm_status_t attach_workspace(void* ws, size_t bytes, size_t need, unsigned** status) {
+    if (!ws || bytes < need || !aligned(ws, 256))
+        return fail(SSM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need);
+    *status = static_cast<unsigned*>(ws);
     return SSM_OK;
 }
 
@@ -271,6 +343,16 @@ namespace ssm {
 // Record a reason for ssm_last_error() on the calling thread and return `s` (for entry points
 // defined in other files of the library).
 ssm_status_t set_error(ssm_status_t s, const char* msg) { return fail(s, "%s", msg); }
+
+cudaError_t record_phase(const ScanArgs& a, int k, bool last, cudaStream_t st) {
+    if (!a.phase_events) return cudaSuccess;
+    const int hi = last ? a.n_phase_events : std::min(k + 1, a.n_phase_events);
+    for (int i = k; i < hi; ++i) {
+        const cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(a.phase_events[i]), st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 }  // namespace ssm
 
 extern "C" {
@@ -286,30 +368,45 @@ ssm_status_t ssm_scan_fwd(const ssm_scan_params* p, void* stream) {
     ssm_status_t s = validate_scan(p, &a);
     if (s != SSM_OK) return s;
     const size_t need = scan_workspace_bytes(a);
-    if (need > 0 && (!a.workspace || a.workspace_bytes < need || !aligned(a.workspace, 256)))
-        return fail(SSM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned", need);
+    if (need > 0) {
+        s = attach_workspace(a.workspace, a.workspace_bytes, need, &a.status);
+        if (s != SSM_OK) return s;
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
     if ((a.debug_flags & SSM_DEBUG_SKIP_FIRST_LOAD) &&
         (a.seqlen <= kShortSeq || a.seqlen > 16 || !ssm::scan_fast_supported(a)))
         return fail(SSM_ERR_INVALID_ARG, "SSM_DEBUG_SKIP_FIRST_LOAD needs %lld < seqlen <= 16 and the TMA path",
                     (long long)kShortSeq);
-    if (a.seqlen == 0) {
-        if (a.h_last) {
-            const size_t bytes = (size_t)(a.batch * a.dim * a.dstate) * sizeof(float);
-            e = a.h0 ? (a.h0 == a.h_last ? cudaSuccess
-                                         : cudaMemcpyAsync(a.h_last, a.h0, bytes, cudaMemcpyDeviceToDevice, st))
-                     : cudaMemsetAsync(a.h_last, 0, bytes, st);
-        }
-    } else if (a.seqlen > kShortSeq && ssm::scan_fast_supported(a)) {
-        e = ssm::launch_scan_fast(a, st);
-    } else if (a.seqlen <= kShortSeq && ssm::scan_decode_supported(a)) {
-        e = ssm::launch_scan_decode(a, st);
+    if (a.seqlen > kShortSeq && ssm::scan_fast_supported(a)) {
+        e = ssm::launch_scan_fast(a, st);   // records its own phase events
     } else {
-        e = ssm::launch_scan_generic(a, st);
+        e = ssm::record_phase(a, 0, false, st);
+        if (e == cudaSuccess) {
+            if (a.seqlen == 0) {
+                if (a.h_last) {
+                    const size_t bytes = (size_t)(a.batch * a.dim * a.dstate) * sizeof(float);
+                    e = a.h0 ? (a.h0 == a.h_last
+                                    ? cudaSuccess
+                                    : cudaMemcpyAsync(a.h_last, a.h0, bytes, cudaMemcpyDeviceToDevice, st))
+                             : cudaMemsetAsync(a.h_last, 0, bytes, st);
+                }
+            } else if (a.seqlen <= kShortSeq && ssm::scan_decode_supported(a)) {
+                e = ssm::launch_scan_decode(a, st);
+            } else {
+                e = ssm::launch_scan_generic(a, st);
+            }
+        }
+        if (e == cudaSuccess) e = ssm::record_phase(a, 1, true, st);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return ok();
+}
+
+size_t ssm_causal_conv1d_workspace_size(const ssm_conv1d_params* p) {
+    ssm::Conv1dArgs a;
+    if (validate_conv1d(p, &a) != SSM_OK) return (size_t)-1;
+    return a.seqlen > 0 ? SSM_WORKSPACE_HEADER_BYTES : 0;
 }
 
 ssm_status_t ssm_causal_conv1d_fwd(const ssm_conv1d_params* p, void* stream) {
@@ -317,6 +414,8 @@ ssm_status_t ssm_causal_conv1d_fwd(const ssm_conv1d_params* p, void* stream) {
     ssm_status_t s = validate_conv1d(p, &a);
     if (s != SSM_OK) return s;
     if (a.seqlen == 0) return ok();
+    s = attach_workspace(p->workspace, p->workspace_bytes, SSM_WORKSPACE_HEADER_BYTES, &a.status);
+    if (s != SSM_OK) return s;
     cudaError_t e = ssm::launch_conv1d(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e);
     return ok();
@@ -325,7 +424,7 @@ ssm_status_t ssm_causal_conv1d_fwd(const ssm_conv1d_params* p, void* stream) {
 size_t ssd_chunk_scan_workspace_size(const ssd_scan_params* p) {
     ssm::SSDArgs a;
     if (validate_ssd(p, &a) != SSM_OK) return (size_t)-1;
-    return 0;
+    return a.seqlen > 0 && ssm::ssd_tc_supported(a) ? SSM_WORKSPACE_HEADER_BYTES : 0;
 }
 
 ssm_status_t ssd_chunk_scan_fwd(const ssd_scan_params* p, void* stream) {
@@ -334,6 +433,10 @@ ssm_status_t ssd_chunk_scan_fwd(const ssd_scan_params* p, void* stream) {
     if (s != SSM_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
+    if (a.seqlen > 0 && ssm::ssd_tc_supported(a)) {
+        s = attach_workspace(a.workspace, a.workspace_bytes, SSM_WORKSPACE_HEADER_BYTES, &a.status);
+        if (s != SSM_OK) return s;
+    }
     if (a.seqlen == 0) {
         if (a.h_last) {
             const size_t bytes = (size_t)(a.batch * a.nheads * a.dstate * a.headdim) * sizeof(float);
@@ -350,11 +453,21 @@ ssm_status_t ssd_chunk_scan_fwd(const ssd_scan_params* p, void* stream) {
     return ok();
 }
 
-ssm_status_t ssm_device_status(void* stream, int clear) {
+ssm_status_t ssm_check_status(void* workspace, void* stream, int clear) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void* ws = workspace;
+    if (!ws) {
+        cudaError_t err = cudaSuccess;
+        ws = ssm::noalloc_scratch(&err);
+        if (!ws) return cuda_fail(err);
+    }
+    if (!aligned(ws, 256)) return fail(SSM_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     unsigned word = 0;
-    cudaError_t e = ssm::read_device_status(&word, clear != 0, static_cast<cudaStream_t>(stream));
+    cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof(unsigned), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess && clear) e = cudaMemsetAsync(ws, 0, sizeof(unsigned), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (word != 0) return fail(static_cast<ssm_status_t>(word), "a kernel latched device status %u", word);
+    if (word != 0) return fail(static_cast<ssm_status_t>(word), "a kernel latched status %u in this workspace", word);
     return ok();
 }
 

@@ -248,7 +248,7 @@ template <bool BF16, bool SILU>
 cudaError_t launch_t(const CUtensorMap& mx, const CUtensorMap& my, const ConvParams& p, int nslices, int per_slice,
                      cudaStream_t st) {
     auto kern = conv1d_kernel<BF16, SILU>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = set_smem_once<conv1d_kernel<BF16, SILU>>(kSmem);
     if (e != cudaSuccess) return e;
     kern<<<dim3((unsigned)nslices, (unsigned)per_slice), kThreads, kSmem, st>>>(mx, my, p);
     note_launches(1);
@@ -275,7 +275,7 @@ cudaError_t launch_conv1d(const Conv1dArgs& a, cudaStream_t st) {
     p.w = a.w;
     p.bias = a.bias;
     p.x_prev = a.x_prev;
-    p.status = device_status_ptr();
+    p.status = a.status;
     if (!p.status) return cudaErrorInvalidValue;
     const int64_t nslices = (a.dim + chan - 1) / chan;
     if (nslices > INT32_MAX) return cudaErrorInvalidValue;

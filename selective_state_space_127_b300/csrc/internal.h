@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "ssmscan.h"
 
 namespace ssm {
@@ -35,6 +37,9 @@ struct ScanArgs {
     const float* conv_b;     // (D) or nullptr
     const void* conv_prev;   // (b, K-1, D) io dtype or nullptr
     int conv_k;
+    unsigned* status;        // the workspace header's status word (nullptr when no workspace)
+    void* const* phase_events;   // cudaEvent_t handles recorded around the launches, or nullptr
+    int n_phase_events;
 };
 
 struct Conv1dArgs {
@@ -47,6 +52,7 @@ struct Conv1dArgs {
     const float* bias;
     const void* x_prev;
     void* y;
+    unsigned* status;        // the workspace header's status word
 };
 
 struct SSDArgs {
@@ -66,10 +72,26 @@ struct SSDArgs {
     float* h_last;
     void* workspace;
     size_t workspace_bytes;
+    unsigned* status;        // the workspace header's status word (tensor-core path)
 };
 
 // Which selective-scan kernel a call takes.
 enum class ScanPath { Generic = 0, Fast = 1, ChunkCarry = 2 };
+
+// Opt kernel KERN into `bytes` (a constant per kernel) of dynamic shared memory above the
+// default 48 KB, once per device: the attribute outlives the call, so later launches skip it.
+template <auto KERN>
+cudaError_t set_smem_once(int bytes) {
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
 
 // Record a reason for ssm_last_error() on the calling thread; returns `s`.
 ssm_status_t set_error(ssm_status_t s, const char* msg);
@@ -77,10 +99,13 @@ ssm_status_t set_error(ssm_status_t s, const char* msg);
 // Count of kernels enqueued by this library (reported through ssm_kernel_launch_count).
 void note_launches(int n);
 
-// Device address of the library's status word on the current device (nullptr on error).
-// Kernels latch SSM_ERR_TIMEOUT there when a bounded wait gives up.
-unsigned* device_status_ptr();
-cudaError_t read_device_status(unsigned* out, bool clear, cudaStream_t st);
+// Record the phase events of a call: before the first launch (k = 0) or after the k-th launch;
+// after the last launch (last = true) every remaining event is recorded too.
+cudaError_t record_phase(const ScanArgs& a, int k, bool last, cudaStream_t st);
+
+// Device address of the status header of the built-in scratch of ssm_scan_fwd_noalloc on the
+// current device (looked up on first use); nullptr with the CUDA error in *err on failure.
+void* noalloc_scratch(cudaError_t* err);
 
 // Kernel launchers: return cudaSuccess or the launch error. They assume valid args.
 cudaError_t launch_conv1d(const Conv1dArgs& a, cudaStream_t st);
@@ -89,7 +114,8 @@ cudaError_t launch_scan_decode(const ScanArgs& a, cudaStream_t st);
 cudaError_t launch_scan_generic(const ScanArgs& a, cudaStream_t s);
 bool scan_fast_supported(const ScanArgs& a);
 // Steps per chunk the fast path uses (a multiple of its tile; >= seqlen when not split) and
-// the workspace it needs for the chunk carries (0 when the sequence is not split).
+// the workspace bytes it needs after the header for the chunk carries (0 when the sequence
+// is not split).
 int64_t scan_fast_chunk(const ScanArgs& a);
 size_t scan_fast_workspace_bytes(const ScanArgs& a);
 cudaError_t launch_scan_fast(const ScanArgs& a, cudaStream_t s);

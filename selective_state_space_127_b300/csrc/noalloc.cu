@@ -11,9 +11,11 @@
 // The buffer is a file-scope device array, so every GPU that loads the library holds it
 // until the process exits. In host code its name does not denote a device address; the
 // address is looked up once per device, with that device current, by cudaGetSymbolAddress,
-// and only that address is handed to the kernels. All calls share the buffer and it keeps
-// the contents of the last call; nothing in it has to start at zero, because the chunked scan
-// writes every element it later reads. Calls whose work overlaps on the GPU race on it.
+// and only that address is handed to the kernels. Like any workspace it starts with the
+// status header (zero when the module loads; ssm_check_status(NULL, ...) reads and clears it)
+// followed by the chunk carries. All calls share the buffer and it keeps the contents of the
+// last call; the carries need no zeroing, because the chunked scan writes every element it
+// later reads. Calls whose work overlaps on the GPU race on it.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -29,6 +31,10 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[SSM_NOALLOC_SCR
 constexpr int kMaxDevices = 64;
 void* g_scratch_addr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
+
+}  // namespace
+
+namespace ssm {
 
 // Device address of g_noalloc_scratch on the current device (looked up on first use).
 cudaError_t scratch_address(void** out) {
@@ -47,7 +53,13 @@ cudaError_t scratch_address(void** out) {
     return cudaSuccess;
 }
 
-}  // namespace
+void* noalloc_scratch(cudaError_t* err) {
+    void* p = nullptr;
+    *err = scratch_address(&p);
+    return *err == cudaSuccess ? p : nullptr;
+}
+
+}  // namespace ssm
 
 extern "C" ssm_status_t ssm_scan_fwd_noalloc(const ssm_scan_params* p, void* stream) {
     const size_t need = ssm_scan_workspace_size(p);
@@ -65,7 +77,7 @@ extern "C" ssm_status_t ssm_scan_fwd_noalloc(const ssm_scan_params* p, void* str
     q.workspace_bytes = 0;
     if (need > 0) {
         void* scratch = nullptr;
-        const cudaError_t e = scratch_address(&scratch);
+        const cudaError_t e = ssm::scratch_address(&scratch);
         if (e != cudaSuccess) {
             char msg[200];
             snprintf(msg, sizeof(msg), "cudaGetSymbolAddress of the built-in scratch: %s", cudaGetErrorString(e));
@@ -76,3 +88,5 @@ extern "C" ssm_status_t ssm_scan_fwd_noalloc(const ssm_scan_params* p, void* str
     }
     return ssm_scan_fwd(&q, stream);
 }
+
+extern "C" size_t ssm_noalloc_scratch_bytes(void) { return (size_t)SSM_NOALLOC_SCRATCH_BYTES; }

@@ -52,7 +52,8 @@ namespace {
 
 // Chunk carry: one thread per (b, d, n) walks the chunks in order,
 //   H_0 = h0,  H_{c+1} = exp(A[d, n] * sumdt_c) * H_c + local_c,
-// and stores H_{c+1} over local_c (the initial state of chunk c + 1).
+// where slot c + 1 holds local_c (pass 1), and stores H_c into slot c: the initial state of
+// every chunk, chunk 0's being a copy of h0 (so that h0 may alias h_last).
 __global__ void scan_carry_kernel(float* carry, const float* sumdt, const float* A, const float* h0,
                                   int64_t batch, int64_t dim, int N, int nsteps) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -63,8 +64,9 @@ __global__ void scan_carry_kernel(float* carry, const float* sumdt, const float*
     const int64_t d = bd % dim;
     const float a = A[d * N + n];
     float H = h0 ? h0[i] : 0.f;
+    carry[i] = H;
     for (int c = 0; c < nsteps; ++c) {
-        const int64_t o = (int64_t)c * total + i;
+        const int64_t o = (int64_t)(c + 1) * total + i;
         H = fmaf(expf(a * sumdt[(int64_t)c * batch * dim + bd]), H, carry[o]);
         carry[o] = H;
     }
@@ -163,7 +165,7 @@ size_t scan_fast_workspace_bytes(const ScanArgs& a) {
     const int64_t q = scan_fast_chunk(a);
     const int64_t nch = (a.seqlen + q - 1) / q;
     if (nch <= 1) return 0;
-    return (size_t)((nch - 1) * a.batch * a.dim * (a.dstate + 1)) * sizeof(float);
+    return (size_t)(nch * a.batch * a.dim * a.dstate + (nch - 1) * a.batch * a.dim) * sizeof(float);
 }
 
 cudaError_t launch_scan_fast(const ScanArgs& a, cudaStream_t st) {
@@ -182,28 +184,35 @@ cudaError_t launch_scan_fast(const ScanArgs& a, cudaStream_t st) {
     const int64_t q = scan_fast_chunk(a);
     const int nch = (int)((a.seqlen + q - 1) / q);
     FastParams fp{a.seqlen, q, (int)a.dim, nch, a.A, a.D, a.bias, a.h0, a.h_last, nullptr, nullptr,
-                  device_status_ptr(), (a.debug_flags & SSM_DEBUG_SKIP_FIRST_LOAD) ? 1 : 0,
+                  a.status, (a.debug_flags & SSM_DEBUG_SKIP_FIRST_LOAD) ? 1 : 0,
                   a.conv_w, a.conv_b, a.conv_prev, a.conv_k};
     if (!fp.status) return cudaErrorInvalidValue;
+    cudaError_t e = record_phase(a, 0, false, st);
+    if (e != cudaSuccess) return e;
     if (nch > 1) {
-        const size_t carry_floats = (size_t)((nch - 1) * a.batch * a.dim * a.dstate);
-        fp.carry = static_cast<float*>(a.workspace);
-        fp.sumdt = fp.carry + carry_floats;
-        cudaError_t e = conv     ? dispatch_conv_pass1(maps, fp, a, nch - 1, st)
-                        : a.zoh ? dispatch_zoh_pass1(maps, fp, a, nch - 1, st)
-                                : dispatch<kPass1, kVarPlain>(maps, fp, a, nch - 1, st);
+        // the carries follow the workspace header
+        const size_t slot_floats = (size_t)(a.batch * a.dim * a.dstate);
+        fp.carry = reinterpret_cast<float*>(static_cast<unsigned char*>(a.workspace) + SSM_WORKSPACE_HEADER_BYTES);
+        fp.sumdt = fp.carry + (size_t)nch * slot_floats;
+        e = conv     ? dispatch_conv_pass1(maps, fp, a, nch - 1, st)
+            : a.zoh ? dispatch_zoh_pass1(maps, fp, a, nch - 1, st)
+                    : dispatch<kPass1, kVarPlain>(maps, fp, a, nch - 1, st);
+        if (e == cudaSuccess) e = record_phase(a, 1, false, st);
         if (e != cudaSuccess) return e;
         const int64_t total = a.batch * a.dim * a.dstate;
         scan_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(fp.carry, fp.sumdt, a.A, a.h0, a.batch,
                                                                           a.dim, a.dstate, nch - 1);
         note_launches(1);
         e = cudaGetLastError();
+        if (e == cudaSuccess) e = record_phase(a, 2, false, st);
         if (e != cudaSuccess) return e;
     }
-    if (conv) return dispatch_conv_full(maps, fp, a, nch, st);
-    if (a.zoh) return dispatch_zoh_full(maps, fp, a, nch, st);
-    if (a.reverse) return dispatch_rev_full(maps, fp, a, nch, st);
-    return dispatch<kFull, kVarPlain>(maps, fp, a, nch, st);
+    e = conv     ? dispatch_conv_full(maps, fp, a, nch, st)
+        : a.zoh ? dispatch_zoh_full(maps, fp, a, nch, st)
+        : a.reverse ? dispatch_rev_full(maps, fp, a, nch, st)
+                    : dispatch<kFull, kVarPlain>(maps, fp, a, nch, st);
+    if (e != cudaSuccess) return e;
+    return record_phase(a, nch > 1 ? 3 : 1, true, st);
 }
 
 }  // namespace ssm

@@ -31,7 +31,9 @@ struct FastParams {
     const float* bias;
     const float* h0;
     float* h_last;
-    float* carry;          // (nchunks - 1, b, D, N): local end states, then initial states
+    float* carry;          // (nchunks, b, D, N): slot c = initial state of chunk c (pass 1 writes
+                           // chunk c's local end state into slot c + 1, the carry kernel turns
+                           // the slots into initial states, slot 0 a copy of h0)
     float* sumdt;          // (nchunks - 1, b, D)
     unsigned* status;
     int skip_first_load;   // test hook: never issue tile 0 (only used when the sequence is one tile)
@@ -158,14 +160,15 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
     const int64_t len = t_end - t_begin;
     const int ntiles = (int)((len + kT - 1) / kT);
 
-    // initial state: h0 for the first chunk, the carried state for the others (pass 2),
-    // zero in pass 1
+    // initial state: h0 when the sequence is one chunk, else the carried state of this chunk
+    // (slot 0 holds a copy of h0, so h0 may be the h_last buffer the last chunk writes); zero
+    // in pass 1
     const float* hinit = nullptr;
     if constexpr (MODE == kFull) {
-        if (chunk == 0)
-            hinit = p.h0 ? p.h0 + ((int64_t)b * p.dim) * N : nullptr;
+        if (p.carry)
+            hinit = p.carry + ((int64_t)chunk * gridDim.y + b) * p.dim * N;
         else
-            hinit = p.carry + ((int64_t)(chunk - 1) * gridDim.y + b) * p.dim * N;
+            hinit = p.h0 ? p.h0 + ((int64_t)b * p.dim) * N : nullptr;
     }
     f2 A2[P], h[P];
     f2 Ainv[ZOH ? P : 1];   // ZOH: 1 / A (0 where A == 0)
@@ -400,7 +403,7 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
             }
         }
     } else {
-        float* out = p.carry + (((int64_t)chunk * gridDim.y + b) * p.dim + d) * N;
+        float* out = p.carry + (((int64_t)(chunk + 1) * gridDim.y + b) * p.dim + d) * N;
 #pragma unroll
         for (int k = 0; k < P; ++k) {
             float lo, hi;
@@ -423,8 +426,10 @@ template <int N, bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS, int MODE, int 
 cudaError_t launch_t(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz, cudaStream_t st) {
     using Lay = Layout<N, BF16, VAR>;
     auto kern = scan_fast_kernel<N, BF16, LPC, GATE, DSKIP, SOFTPLUS, MODE, VAR>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kTotal);
-    if (e != cudaSuccess) return e;
+    if constexpr (Lay::kTotal > 48 * 1024) {
+        cudaError_t e = set_smem_once<scan_fast_kernel<N, BF16, LPC, GATE, DSKIP, SOFTPLUS, MODE, VAR>>(Lay::kTotal);
+        if (e != cudaSuccess) return e;
+    }
     dim3 grid((unsigned)((a.dim + kCh - 1) / kCh), (unsigned)a.batch, (unsigned)nz);
     kern<<<grid, kCh * LPC, Lay::kTotal, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], fp);
     note_launches(1);

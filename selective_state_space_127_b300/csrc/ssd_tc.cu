@@ -666,9 +666,9 @@ cudaError_t launch_ssd_tc(const SSDArgs& a, cudaStream_t st) {
     p.bias = a.bias;
     p.h0 = a.h0;
     p.h_last = a.h_last;
-    p.status = device_status_ptr();
+    p.status = a.status;
     if (!p.status) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(ssd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = set_smem_once<ssd_tc_kernel>(kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)a.nheads, (unsigned)a.batch);
     ssd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mX, mB, mC, mY, p);

@@ -44,7 +44,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
 }
 
 // Wait for phase `parity` of `bar` to complete, for at most kWaitBudgetNs. Returns false
-// (after latching SSM_ERR_TIMEOUT in the library's device status word) if the budget ran out.
+// (after latching SSM_ERR_TIMEOUT in the status word of the call's workspace) if the budget ran out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity, unsigned* status) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();

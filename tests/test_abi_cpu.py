@@ -75,9 +75,9 @@ def _valid_scan_params():
     p.batch, p.seqlen, p.dim, p.dstate = 2, 8, 4, 16
     p.io_dtype = binding.SSM_DTYPE_BF16
     p.delta_softplus = 1
-    fake = 1 << 20  # an aligned, never-dereferenced address: validation only
-    for name in ("x", "delta", "B", "C", "A", "y"):
-        setattr(p, name, fake)
+    # aligned, never-dereferenced, non-overlapping addresses: validation only
+    for i, name in enumerate(("x", "delta", "B", "C", "A", "y")):
+        setattr(p, name, (i + 1) << 20)
     p.x_stride[:] = (32, 4, 1)
     p.delta_stride[:] = (32, 4, 1)
     p.y_stride[:] = (32, 4, 1)
@@ -111,6 +111,69 @@ def test_invalid_scan_args_are_rejected_before_launch(lib, field, value, status)
     assert lib.ssm_scan_workspace_size(ctypes.byref(p)) == ctypes.c_size_t(-1).value
     assert lib.ssm_scan_fwd(ctypes.byref(p), None) == status
     assert lib.ssm_last_error().decode() != ""
+
+
+def _header_define(name):
+    m = re.search(r"#define\s+" + name + r"\s+(.+)", open(HEADER).read())
+    return eval(m.group(1).replace("u", ""))
+
+
+def test_header_constants_match_the_library_and_binding(lib):
+    assert lib.ssm_noalloc_scratch_bytes() == _header_define("SSM_NOALLOC_SCRATCH_BYTES")
+    assert binding.noalloc_scratch_bytes() == _header_define("SSM_NOALLOC_SCRATCH_BYTES")
+    assert binding.WORKSPACE_HEADER_BYTES == _header_define("SSM_WORKSPACE_HEADER_BYTES")
+    assert binding.ABI_VERSION == _header_define("SSMSCAN_ABI_VERSION")
+
+
+@pytest.mark.parametrize("name", ["x", "delta", "B", "C", "A"])
+def test_output_overlapping_an_input_is_rejected(lib, name):
+    p = _valid_scan_params()
+    p.y = getattr(p, name) + 32           # y's range starts inside the input's range
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
+    assert "overlap" in lib.ssm_last_error().decode()
+    p = _valid_scan_params()
+    p.h_last = getattr(p, name)           # the final state over an input
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
+
+
+def test_h_last_may_be_h0_but_not_partly_overlap_it(lib):
+    p = _valid_scan_params()
+    p.h0 = p.h_last = 7 << 20
+    assert lib.ssm_scan_workspace_size(ctypes.byref(p)) != ctypes.c_size_t(-1).value
+    p.h_last = (7 << 20) + 64
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
+
+
+def test_phase_event_fields_are_checked(lib):
+    p = _valid_scan_params()
+    p.n_phase_events = 2                  # no array
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
+    p = _valid_scan_params()
+    p.reserved3 = 1
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
+
+
+def test_workspace_sizes_include_the_status_header(lib):
+    p = _valid_scan_params()              # bf16, dense, 16-byte aligned: the TMA path
+    p.seqlen = 64
+    p.x_stride[:] = p.delta_stride[:] = p.y_stride[:] = (64 * 16, 16, 1)
+    p.dim = 16
+    p.B_stride[:] = p.C_stride[:] = (64 * 16, 16, 1)
+    # the TMA path needs the driver's tensor-map encoder; without a driver (a CPU-only host)
+    # the library picks the generic kernel, which needs no workspace
+    n1 = lib.ssm_scan_workspace_size(ctypes.byref(p))
+    p.chunk_len = 32                      # two chunks: carries after the header
+    n2 = lib.ssm_scan_workspace_size(ctypes.byref(p))
+    if n1 != 0:
+        assert n1 == binding.WORKSPACE_HEADER_BYTES
+        assert n2 == binding.WORKSPACE_HEADER_BYTES + (2 * 2 * 16 * 16 + 1 * 2 * 16) * 4
+    else:
+        assert n2 == 0
+    p.seqlen = 1                          # the short-sequence kernel has no device-side waits
+    assert lib.ssm_scan_workspace_size(ctypes.byref(p)) == 0
+    c = _valid_conv_params()
+    assert lib.ssm_causal_conv1d_workspace_size(ctypes.byref(c)) == binding.WORKSPACE_HEADER_BYTES
+    assert lib.ssm_causal_conv1d_fwd(ctypes.byref(c), None) == binding.SSM_ERR_WORKSPACE
 
 
 def test_overlapping_output_strides_are_rejected(lib):

@@ -12,7 +12,7 @@ def test_reference_arm_prints_one_contract_line(monkeypatch, capsys):
     sys.path.insert(0, ROOT)
     import bench
 
-    # a small sample of workload 1 (one batch row, eight channels, all 2048 steps, one thread)
+    # a small sample of the headline workload (one batch row, eight channels, all steps, one thread)
     monkeypatch.setattr(bench, "_oracle_sample", lambda w, target_s: (1, 8, 1))
     monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--steps", "2", "--warmup", "3"])
     monkeypatch.delenv("RANK", raising=False)
@@ -25,7 +25,7 @@ def test_reference_arm_prints_one_contract_line(monkeypatch, capsys):
     assert d["unit"] == "GB/s" and d["value"] > 0 and d["higher_is_better"] is True
     assert d["steps"] == 2 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["dtype"] == "f64" and d["vs_baseline"] is None and d["scaling"] == "weak"
-    assert d["config"]["workload"].startswith("mamba130m-layer b8 D1536 L2048 N16")
+    assert d["config"]["workload"].startswith("long-seq b1 D2048 L131072 N16")
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from selective_state_space_127_b300 import binding, causal_conv1d_fwd, device_status, ssm_scan_fwd
+from selective_state_space_127_b300 import binding, causal_conv1d_fwd, check_status, new_workspace, ssm_scan_fwd
 from selective_state_space_127_b300.synth import make_scan_inputs
 from conftest import rel_l2
 
@@ -97,7 +97,8 @@ def test_fused_prologue_matches_oracle_on_both_paths(cuda_dev, b, L, D, N, dt, K
     g = _to(cuda_dev, inp)
     cw = dict(conv_weight=w.to(cuda_dev), conv_bias=cb.to(cuda_dev),
               conv_x_prev=prev.to(cuda_dev) if prev is not None else None)
-    y_fast, h_fast = ssm_scan_fwd(**g, chunk_len=chunk, **cw)
+    ws = new_workspace(binding.scan_workspace_size(**g, chunk_len=chunk, **cw), cuda_dev)
+    y_fast, h_fast = ssm_scan_fwd(**g, chunk_len=chunk, workspace=ws, **cw)
     y_gen, h_gen = ssm_scan_fwd(**dict(g, x=_misaligned_copy(g["x"])), **cw)
     torch.cuda.synchronize()
     y_ref, h_ref = _fused_ref(inp, w, cb, prev)
@@ -105,7 +106,7 @@ def test_fused_prologue_matches_oracle_on_both_paths(cuda_dev, b, L, D, N, dt, K
     assert rel_l2(h_fast.cpu().numpy(), h_ref) <= TOL_H[dt]
     assert rel_l2(y_gen.float().cpu().numpy(), y_ref) <= TOL[dt]
     assert rel_l2(h_gen.cpu().numpy(), h_ref) <= TOL_H[dt]
-    assert device_status() == binding.SSM_OK
+    assert check_status(ws) == binding.SSM_OK
 
 
 def test_fused_prologue_split_and_resume(cuda_dev):

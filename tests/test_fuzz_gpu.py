@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from selective_state_space_127_b300 import binding, device_status, ssm_scan_fwd
+from selective_state_space_127_b300 import binding, check_status, new_workspace, ssm_scan_fwd
 from selective_state_space_127_b300.synth import make_scan_inputs
 from conftest import rel_l2
 
@@ -57,13 +57,15 @@ def test_random_configuration_matches_oracle(cuda_dev, i):
         conv = dict(conv_weight=w.to(cuda_dev), conv_bias=cb.to(cuda_dev))
         x_ref = oracle.causal_conv1d_ref(inp["x"], w, cb)
     dev_inp = {k: (v.to(cuda_dev) if v is not None else None) for k, v in inp.items()}
-    y, h = ssm_scan_fwd(**dev_inp, h0=h0.to(cuda_dev) if h0 is not None else None, **kw, **conv)
+    h0_d = h0.to(cuda_dev) if h0 is not None else None
+    ws = new_workspace(binding.scan_workspace_size(**dev_inp, h0=h0_d, **kw, **conv), cuda_dev)
+    y, h = ssm_scan_fwd(**dev_inp, h0=h0_d, workspace=ws, **kw, **conv)
     torch.cuda.synchronize()
     y_ref, h_ref = oracle.ssm_scan_ref(**dict(inp, x=x_ref), h0=h0, delta_softplus=c["softplus"], zoh=c["zoh"],
                                        reverse=c["reverse"])
     assert rel_l2(y.float().cpu().numpy(), y_ref) <= TOL_Y[c["dt"]], c
     assert rel_l2(h.cpu().numpy(), h_ref) <= TOL_H[c["dt"]], c
-    assert device_status() == binding.SSM_OK
+    assert check_status(ws) == binding.SSM_OK
 
 
 def _ssd_config(i):
@@ -85,11 +87,13 @@ def test_random_ssd_configuration_matches_oracle(cuda_dev, i):
                           d_skip="normal" if c["dskip"] else "none", gate=c["gate"], ngroups=c["G"])
     h0 = torch.randn(c["b"], c["H"], c["N"], c["P"], generator=torch.Generator().manual_seed(9700 + i)) if c["h0"] else None
     dev_inp = {k: (v.to(cuda_dev) if v is not None else None) for k, v in inp.items()}
-    y, h = ssd_chunk_scan_fwd(**dev_inp, chunk_size=c["Q"], h0=h0.to(cuda_dev) if h0 is not None else None)
+    ws = new_workspace(binding.WORKSPACE_HEADER_BYTES, cuda_dev)
+    y, h = ssd_chunk_scan_fwd(**dev_inp, chunk_size=c["Q"], h0=h0.to(cuda_dev) if h0 is not None else None,
+                              workspace=ws)
     torch.cuda.synchronize()
     y_ref, h_ref = oracle.ssd_scan_ref(**inp, h0=h0)
     # the tensor-core kernel (bf16, P = 64, N = 128) carries bf16 operands: h within 5e-3
     tol_h = 5e-3 if c["dt"] == "bf16" else 1e-5
     assert rel_l2(y.float().cpu().numpy(), y_ref) <= TOL_Y[c["dt"]], c
     assert rel_l2(h.cpu().numpy(), h_ref) <= tol_h, c
-    assert device_status() == binding.SSM_OK
+    assert check_status(ws) == binding.SSM_OK

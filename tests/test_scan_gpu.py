@@ -155,29 +155,59 @@ def test_split_and_resume_on_gpu(cuda_dev):
     assert rel_l2(h2.cpu().numpy(), h.cpu().numpy()) <= 1e-6
 
 
-def _sampled_parity(k, dev, n_chan=48, seed=0):
+def full_tensor_parity(k, dev, slice_ch=512):
+    """Scan workload k at full size on the GPU (with the chunking the benchmark uses), then the
+    oracle over every channel, a slice of channels at a time (bounded host memory). Returns
+    the rel-L2 of y and h_last over the whole tensors, the largest element-wise excess over
+    the element bounds (<= 0 means every element is within them), and the fraction of y
+    elements that equal the oracle rounded to bf16.
+
+    Element bounds: |y - y_ref| <= 2^-7 |y_ref| + 1e-3 rms(y_ref) (two bf16 steps, plus fp32
+    noise where y is near zero); |h - h_ref| <= 1e-3 |h_ref| + 1e-4 rms(h_ref)."""
     w = SCAN_WORKLOADS[k]
     inp = scan_workload_inputs(k, device=dev)
     y, h = ssm_scan_fwd(**inp, chunk_len=w.chunk_len)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(seed)
-    idx = torch.tensor(np.sort(rng.choice(w.dim, size=min(n_chan, w.dim), replace=False)), device=dev)
-    sub = {k2: (v.index_select(2, idx) if k2 in ("x", "delta", "z") else v) for k2, v in inp.items()}
-    sub["A"] = inp["A"].index_select(0, idx)
-    sub["D"] = inp["D"].index_select(0, idx) if inp["D"] is not None else None
-    sub["delta_bias"] = inp["delta_bias"].index_select(0, idx)
-    y_ref, h_ref = oracle.ssm_scan_ref(**{k2: (v.cpu() if v is not None else None) for k2, v in sub.items()})
-    y_s = y.index_select(2, idx).float().cpu().numpy()
-    h_s = h.index_select(1, idx).cpu().numpy()
-    return rel_l2(y_s, y_ref), rel_l2(h_s, h_ref)
+    acc = dict(ny=0.0, dy=0.0, nh=0.0, dh=0.0, excess_y=-np.inf, excess_h=-np.inf, same=0, count=0)
+    for d0 in range(0, w.dim, slice_ch):
+        d1 = min(w.dim, d0 + slice_ch)
+        sub = {k2: (v[:, :, d0:d1].cpu() if k2 in ("x", "delta", "z") else v) for k2, v in inp.items()}
+        sub["B"], sub["C"] = inp["B"].cpu(), inp["C"].cpu()
+        sub["A"] = inp["A"][d0:d1].cpu()
+        sub["D"] = inp["D"][d0:d1].cpu() if inp["D"] is not None else None
+        sub["delta_bias"] = inp["delta_bias"][d0:d1].cpu()
+        y_ref, h_ref = oracle.ssm_scan_ref(**sub)
+        y_s = y[:, :, d0:d1].float().cpu().numpy().astype(np.float64)
+        h_s = h[:, d0:d1].cpu().numpy().astype(np.float64)
+        rms_y = np.sqrt(np.mean(y_ref ** 2))
+        rms_h = np.sqrt(np.mean(h_ref ** 2))
+        ey = np.abs(y_s - y_ref) - (2.0 ** -7 * np.abs(y_ref) + 1e-3 * rms_y)
+        eh = np.abs(h_s - h_ref) - (1e-3 * np.abs(h_ref) + 1e-4 * rms_h)
+        acc["excess_y"] = max(acc["excess_y"], float(ey.max()))
+        acc["excess_h"] = max(acc["excess_h"], float(eh.max()))
+        acc["ny"] += float(((y_s - y_ref) ** 2).sum())
+        acc["dy"] += float((y_ref ** 2).sum())
+        acc["nh"] += float(((h_s - h_ref) ** 2).sum())
+        acc["dh"] += float((h_ref ** 2).sum())
+        y_b = torch.from_numpy(y_ref).to(torch.bfloat16)
+        acc["same"] += int((y[:, :, d0:d1].cpu() == y_b).sum())
+        acc["count"] += y_ref.size
+    return (np.sqrt(acc["ny"] / acc["dy"]), np.sqrt(acc["nh"] / acc["dh"]), acc["excess_y"], acc["excess_h"],
+            acc["same"] / acc["count"])
 
 
 @pytest.mark.parametrize("k", [1, 2, 3])
-def test_full_size_workloads_on_sampled_channels(cuda_dev, k):
-    ey, eh = _sampled_parity(k, cuda_dev, n_chan=32 if k == 3 else 64, seed=k)
-    print(f"workload {k}: rel-L2 y {ey:.3e}  h_last {eh:.3e}")
+def test_full_size_workloads_whole_tensors(cuda_dev, k):
+    """Every element of y and h_last of the full-size workloads against the oracle: rel-L2
+    over the whole tensors and an element-wise bound, so an error confined to one channel
+    tile, one batch row or one chunk boundary fails."""
+    ey, eh, xy, xh, same = full_tensor_parity(k, cuda_dev)
+    print(f"workload {k}: rel-L2 y {ey:.3e} h_last {eh:.3e}; element excess y {xy:.2e} h {xh:.2e}; "
+          f"y equal to the rounded oracle {same:.4f}")
     assert ey <= TOL_Y["bf16"]
     assert eh <= TOL_H["bf16"]
+    assert xy <= 0.0 and xh <= 0.0
+    assert same >= 0.9
 
 
 def test_invalid_args_raise_without_launch(cuda_dev):

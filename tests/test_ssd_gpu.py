@@ -73,24 +73,45 @@ def test_h0_and_chunk_size_invariance(cuda_dev):
         assert rel_l2(y, outs[0][0]) <= 1e-2
 
 
-def test_full_size_workload_on_sampled_heads(cuda_dev):
+def test_full_size_workload_whole_tensors(cuda_dev):
+    """Every element of y and h_last of the full-size SSD workload against the oracle, a slice
+    of heads at a time: rel-L2 over the whole tensors and an element-wise bound, so an error
+    confined to one head, one batch row or one block fails.
+
+    The bound is the usual one for sums of rounded products: the tensor-core path rounds the
+    MMA operands (the masked decayed C B^T block, w*x, the carried state) to bf16, a relative
+    error of at most 2^-9 per term, so |y - y_ref| <= 2^-6 y_abs + 2^-8 |y_ref| (terms plus the
+    final rounding of y to bf16) and |h - h_ref| <= 2^-6 h_abs, where y_abs and h_abs are the
+    oracle run on |x|, |B|, |C|: the sums of the terms' magnitudes."""
     w = SSD_WORKLOAD
     inp = ssd_workload_inputs(device=cuda_dev)
     y, h = ssd_chunk_scan_fwd(**inp, chunk_size=w.chunk)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(4)
-    heads = torch.tensor(np.sort(rng.choice(w.nheads, size=6, replace=False)), device=cuda_dev)
-    sub = dict(inp)
-    sub["x"] = inp["x"].index_select(2, heads)
-    sub["delta"] = inp["delta"].index_select(2, heads)
-    sub["A"] = inp["A"].index_select(0, heads)
-    sub["delta_bias"] = inp["delta_bias"].index_select(0, heads)
-    y_ref, h_ref = oracle.ssd_scan_ref(**{k: (v.cpu() if v is not None else None) for k, v in sub.items()})
-    ey = rel_l2(y.index_select(2, heads).float().cpu().numpy(), y_ref)
-    eh = rel_l2(h.index_select(1, heads).cpu().numpy(), h_ref)
-    print(f"SSD workload: rel-L2 y {ey:.3e}  h_last {eh:.3e}")
+    ny = dy = nh = dh = 0.0
+    excess_y = excess_h = -np.inf
+    for h0 in range(0, w.nheads, 16):
+        h1 = min(w.nheads, h0 + 16)
+        sub = dict(inp)
+        sub["x"] = inp["x"][:, :, h0:h1]
+        sub["delta"] = inp["delta"][:, :, h0:h1]
+        sub["A"] = inp["A"][h0:h1]
+        sub["delta_bias"] = inp["delta_bias"][h0:h1]
+        host = {k: (v.cpu() if v is not None else None) for k, v in sub.items()}
+        y_ref, h_ref = oracle.ssd_scan_ref(**host)
+        y_abs, h_abs = oracle.ssd_scan_ref(**dict(host, x=host["x"].abs(), B=host["B"].abs(), C=host["C"].abs()))
+        y_s = y[:, :, h0:h1].float().cpu().numpy().astype(np.float64)
+        h_s = h[:, h0:h1].cpu().numpy().astype(np.float64)
+        excess_y = max(excess_y, float((np.abs(y_s - y_ref) - (2.0 ** -6 * y_abs + 2.0 ** -8 * np.abs(y_ref))).max()))
+        excess_h = max(excess_h, float((np.abs(h_s - h_ref) - 2.0 ** -6 * h_abs).max()))
+        ny += float(((y_s - y_ref) ** 2).sum())
+        dy += float((y_ref ** 2).sum())
+        nh += float(((h_s - h_ref) ** 2).sum())
+        dh += float((h_ref ** 2).sum())
+    ey, eh = np.sqrt(ny / dy), np.sqrt(nh / dh)
+    print(f"SSD workload: rel-L2 y {ey:.3e} h_last {eh:.3e}; element excess y {excess_y:.2e} h {excess_h:.2e}")
     assert ey <= TOL_Y["bf16"]
     assert eh <= TOL_H["bf16"]
+    assert excess_y <= 0.0 and excess_h <= 0.0
 
 
 TC_CASES = [
