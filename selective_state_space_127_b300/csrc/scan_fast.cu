@@ -14,15 +14,17 @@
 // through TMA stores from a double buffer. B and C tiles are widened to fp32 once per tile
 // by the CTA, so lanes then read their states' values with 8- or 16-byte loads.
 //
-// Steps go in groups of LPC. Lane g of a channel computes the per-(t, channel) scalars of
-// step g of the group (dt = softplus(delta + bias), dt x, silu(z), D x) one group ahead, so
-// that chain overlaps the state updates of the current group; the (dt, dt x) pairs are then
+// Steps go in supergroups of 2 LPC. Lane g of a channel computes the per-(t, channel) scalars
+// of steps g and g + LPC of the supergroup (dt = softplus(delta + bias), dt x, silu(z), D x)
+// as packed pairs (f32x2 arithmetic, a branch-free softplus) one supergroup ahead, so that
+// chain overlaps the state updates of the current supergroup; the (dt, dt x) values are then
 // broadcast inside the channel's lanes. Per step and state:
 //   A_bar[n] = 2^(dt * A[n] * log2 e)           SFU ex2
 //   h[n] = A_bar[n] h[n] + (dt x) B[n]          packed fp32 pairs (fma.rn.f32x2)
 //   y += C[n] h[n]                               packed pairs
-// and the lanes' partial sums of the LPC steps are reduce-scattered (log2 LPC shuffle
-// rounds), leaving lane g with step g's y, which it finishes as (y + D x) silu(z).
+// and the lanes' partial sums of each half of the supergroup are reduce-scattered (log2 LPC
+// shuffle rounds), leaving lane g with the y of steps g and g + LPC, which it finishes as
+// (y + D x) silu(z) on the pair.
 //
 // Chunked sequence (long sequences with few channels, where one CTA per channel tile
 // would leave most SMs idle):

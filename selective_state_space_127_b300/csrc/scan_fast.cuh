@@ -77,38 +77,77 @@ __device__ __forceinline__ float ld_io(const void* base, int i, bool bf16) {
     return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]) : static_cast<const float*>(base)[i];
 }
 
-// Per-(step, channel) scalars one lane computes for its step of a group.
-struct Scal {
-    float dt, u, dx, gate;
+// softplus(v) = log(1 + e^v) of both halves of a pair, without a branch: max(v, 0) + log1p(e)
+// with e = e^-|v| in (0, 1] from the SFU, and log1p(e) = 2 atanh(s), s = e / (2 + e) in
+// (0, 1/3], summed as 2 s (1 + s^2/3 + s^4/5 + ... + s^12/13): the first omitted term, s^15/15,
+// is below 1.5e-8 relative, and the series keeps full relative accuracy for the small steps
+// (softplus near e^v) where log(1 + e) itself would cancel.
+__device__ __forceinline__ f2 softplus2(f2 v) {
+    float v0, v1;
+    upk(v, v0, v1);
+    const f2 e = pk(ex2_approx(-fabsf(v0) * kLog2e), ex2_approx(-fabsf(v1) * kLog2e));
+    float d0, d1;
+    upk(add2(e, pk(2.f, 2.f)), d0, d1);
+    const f2 sv = mul2(e, pk(rcp_approx(d0), rcp_approx(d1)));
+    const f2 w = mul2(sv, sv);
+    f2 q = fma2(w, pk(2.f / 13.f, 2.f / 13.f), pk(2.f / 11.f, 2.f / 11.f));
+    q = fma2(w, q, pk(2.f / 9.f, 2.f / 9.f));
+    q = fma2(w, q, pk(2.f / 7.f, 2.f / 7.f));
+    q = fma2(w, q, pk(2.f / 5.f, 2.f / 5.f));
+    q = fma2(w, q, pk(2.f / 3.f, 2.f / 3.f));
+    q = fma2(w, q, pk(2.f, 2.f));
+    return add2(mul2(sv, q), pk(fmaxf(v0, 0.f), fmaxf(v1, 0.f)));
+}
+
+// silu(z) = z / (1 + e^-z) of both halves of a pair (SFU ex2 and rcp).
+__device__ __forceinline__ f2 silu2(f2 z) {
+    float a0, a1;
+    upk(mul2(z, pk(-kLog2e, -kLog2e)), a0, a1);
+    float d0, d1;
+    upk(add2(pk(ex2_approx(a0), ex2_approx(a1)), pk(1.f, 1.f)), d0, d1);
+    return mul2(z, pk(rcp_approx(d0), rcp_approx(d1)));
+}
+
+// Per-(step, channel) scalars of two steps of one channel as packed pairs (lo: the first):
+// dt = softplus(delta + bias), the input term u = dt x, the skip D x and the gate silu(z).
+struct Scal2 {
+    f2 dt, u, dx, gate;
 };
 
-// Conv prologue taps of one channel, right-aligned: w[3] multiplies x_t, w[0] x_{t-3}.
-struct ConvTaps {
-    float w[4];
-    float b;
+// Conv prologue taps of one channel, right-aligned (w[3] multiplies x_t, w[0] x_{t-3}), each
+// duplicated into a pair.
+struct ConvTaps2 {
+    f2 w[4];
+    f2 b;
 };
 
-// With VAR == kVarZoh, u carries x itself (the ZOH input coefficient depends on the state).
+// The scalars of tile rows j0 and j1 (row validity v0, v1: a step past the end of the sequence
+// gets dt = 0, which leaves the state unchanged). With VAR == kVarZoh, u carries x itself (the
+// ZOH input coefficient depends on the state).
 template <bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS, int VAR>
-__device__ __forceinline__ Scal scalars(const void* xs, const void* ds, const void* zs, int jj, int c, float bias,
-                                        float Dd, bool tv, const ConvTaps& ct) {
-    Scal r;
-    float xr;
+__device__ __forceinline__ Scal2 scalars2(const void* xs, const void* ds, const void* zs, int j0, int j1, int c,
+                                          f2 bias2, f2 D2, bool v0, bool v1, const ConvTaps2& ct) {
+    Scal2 r;
+    f2 x2;
     if constexpr (VAR == kVarConv) {
-        // the x tile starts kHalo rows early: rows jj .. jj + 3 hold x_{t-3} .. x_t
-        float v = ct.b;
+        // the x tile starts kHalo rows early: rows j .. j + 3 hold x_{t-3} .. x_t
+        f2 v = ct.b;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v = fmaf(ct.w[j], ld_io(xs, (jj + j) * kCh + c, BF16), v);
-        xr = silu_fast(v);
+        for (int j = 0; j < 4; ++j)
+            v = fma2(ct.w[j], pk(ld_io(xs, (j0 + j) * kCh + c, BF16), ld_io(xs, (j1 + j) * kCh + c, BF16)), v);
+        x2 = silu2(v);
     } else {
-        xr = ld_io(xs, jj * kCh + c, BF16);
+        x2 = pk(ld_io(xs, j0 * kCh + c, BF16), ld_io(xs, j1 * kCh + c, BF16));
     }
-    float dt = ld_io(ds, jj * kCh + c, BF16) + bias;
-    if constexpr (SOFTPLUS) dt = softplus_fast(dt);
-    r.dt = tv ? dt : 0.f;
-    r.u = VAR == kVarZoh ? (tv ? xr : 0.f) : r.dt * xr;
-    r.dx = DSKIP ? Dd * xr : 0.f;
-    r.gate = GATE ? silu_fast(ld_io(zs, jj * kCh + c, BF16)) : 1.f;
+    f2 dt = add2(pk(ld_io(ds, j0 * kCh + c, BF16), ld_io(ds, j1 * kCh + c, BF16)), bias2);
+    if constexpr (SOFTPLUS) dt = softplus2(dt);
+    float t0, t1, x0, x1;
+    upk(dt, t0, t1);
+    upk(x2, x0, x1);
+    r.dt = pk(v0 ? t0 : 0.f, v1 ? t1 : 0.f);
+    r.u = VAR == kVarZoh ? pk(v0 ? x0 : 0.f, v1 ? x1 : 0.f) : mul2(r.dt, x2);
+    r.dx = DSKIP ? mul2(D2, x2) : pk(0.f, 0.f);
+    r.gate = GATE ? silu2(pk(ld_io(zs, j0 * kCh + c, BF16), ld_io(zs, j1 * kCh + c, BF16))) : pk(1.f, 1.f);
     return r;
 }
 
@@ -171,7 +210,7 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
             hinit = p.h0 ? p.h0 + ((int64_t)b * p.dim) * N : nullptr;
     }
     f2 A2[P], h[P];
-    f2 Ainv[ZOH ? P : 1];   // ZOH: 1 / A (0 where A == 0)
+    f2 Ainv[ZOH ? P : 1], nAinv[ZOH ? P : 1];   // ZOH: 1 / A and -1 / A (0 where A == 0)
 #pragma unroll
     for (int k = 0; k < P; ++k) {
         const int n = g * S + 2 * k;
@@ -184,21 +223,32 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
                 h1v = hinit[(int64_t)d * N + n + 1];
             }
         }
-        if constexpr (ZOH) Ainv[k] = pk(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
+        if constexpr (ZOH) {
+            Ainv[k] = pk(a0 != 0.f ? 1.f / a0 : 0.f, a1 != 0.f ? 1.f / a1 : 0.f);
+            nAinv[k] = pk(a0 != 0.f ? -1.f / a0 : 0.f, a1 != 0.f ? -1.f / a1 : 0.f);
+        }
         A2[k] = pk(a0 * kLog2e, a1 * kLog2e);
         h[k] = pk(h0v, h1v);
     }
     const float bias = (dvalid && p.bias) ? p.bias[d] : 0.f;
     const float Dd = (DSKIP && dvalid) ? p.D[d] : 0.f;
+    const f2 bias2 = pk(bias, bias), D2 = pk(Dd, Dd);
     float dtsum = 0.f;   // pass 1: sum of dt over the chunk
-    ConvTaps ct{{0.f, 0.f, 0.f, 0.f}, 0.f};
+    ConvTaps2 ct;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ct.w[j] = pk(0.f, 0.f);
+    ct.b = pk(0.f, 0.f);
     if constexpr (CONV) {
         if (dvalid) {
             const int K = p.conv_k;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                if (j >= 4 - K) ct.w[j] = p.conv_w[(int64_t)d * K + j - (4 - K)];
-            ct.b = p.conv_b ? p.conv_b[d] : 0.f;
+                if (j >= 4 - K) {
+                    const float w = p.conv_w[(int64_t)d * K + j - (4 - K)];
+                    ct.w[j] = pk(w, w);
+                }
+            const float cb = p.conv_b ? p.conv_b[d] : 0.f;
+            ct.b = pk(cb, cb);
         }
     }
 
@@ -294,24 +344,31 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         // processing step k of the tile is its row rr(k): the rows run backwards in reverse
         auto rr = [](int k) { return REV ? kT - 1 - k : k; };
 
-        float yout[kT / LPC];   // the steps this lane finishes; stored after the loop so that no
-                                // shared-memory store sits between the loads of later steps
-        Scal cur = scalars<BF16, kGate, DSKIP && kReadout, SOFTPLUS, VAR>(xs, ds, zs, rr(g), c, bias, Dd,
-                                                                          rr(g) < tcount, ct);
+        // Steps go in supergroups of 2 LPC: lane g forms the scalars of steps g and g + LPC of
+        // each (as one packed pair) one supergroup ahead, and finishes the outputs of those
+        // same two steps.
+        constexpr int kSG = 2 * LPC;
+        constexpr int kNSG = kT / kSG;
+        f2 yout[kNSG];   // the steps this lane finishes; stored after the loop so that no
+                         // shared-memory store sits between the loads of later steps
+        auto scal_at = [&](int sg) {
+            const int r0 = rr(sg * kSG + g), r1 = rr(sg * kSG + g + LPC);
+            return scalars2<BF16, kGate, DSKIP && kReadout, SOFTPLUS, VAR>(xs, ds, zs, r0, r1, c, bias2, D2,
+                                                                          r0 < tcount, r1 < tcount, ct);
+        };
+        Scal2 cur = scal_at(0);
 #pragma unroll
-        for (int grp = 0; grp < kT / LPC; ++grp) {
-            // the next group's scalars: independent of the state, overlaps the updates below
-            const int jn = (grp + 1) * LPC + g;
-            const Scal nxt = scalars<BF16, kGate, DSKIP && kReadout, SOFTPLUS, VAR>(
-                xs, ds, zs, jn < kT ? rr(jn) : rr(g), c, bias, Dd, jn < kT && rr(jn) < tcount, ct);
-            float acc[LPC];
+        for (int sg = 0; sg < kNSG; ++sg) {
+            // the next supergroup's scalars: independent of the state, overlaps the updates below
+            const Scal2 nxt = sg + 1 < kNSG ? scal_at(sg + 1) : cur;
+            float acc[kSG];
 #pragma unroll
-            for (int q = 0; q < LPC; ++q) {
-                const float dtq = __shfl_sync(0xffffffffu, cur.dt, q, LPC);
-                const float uq = __shfl_sync(0xffffffffu, cur.u, q, LPC);
+            for (int q = 0; q < kSG; ++q) {
+                const float dtq = __shfl_sync(0xffffffffu, q < LPC ? lo_of(cur.dt) : hi_of(cur.dt), q % LPC, LPC);
+                const float uq = __shfl_sync(0xffffffffu, q < LPC ? lo_of(cur.u) : hi_of(cur.u), q % LPC, LPC);
                 if constexpr (MODE == kPass1) dtsum += dtq;
                 const f2 dt2 = pk(dtq, dtq), u2 = pk(uq, uq);
-                const int row = rr(grp * LPC + q);
+                const int row = rr(sg * kSG + q);
                 f2 bv[P];
                 lds_pairs<S>(Bf + row * N + g * S, bv);
                 f2 cv[P];
@@ -325,19 +382,20 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
                     const f2 ab = pk(ex2_approx(e0), ex2_approx(e1));
                     f2 ub;
                     if constexpr (ZOH) {
-                        // B_bar x = c B x with c = (A_bar - 1) / A; for |z| = |dt A| < 1/8 the
-                        // series dt (1 + z/2 + z^2/6 + z^3/24 + z^4/120) (no cancellation; the
-                        // dropped z^5/720 term is below 5e-8 relative), else (A_bar - 1) (1 / A)
+                        // B_bar x = c B x with c = (A_bar - 1) / A = dt phi(z), z = dt A. For
+                        // |z| < 1/16 the series phi = 1 + z/2 + z^2/6 + z^3/24 (no cancellation;
+                        // the dropped z^4/120 term is below 1.3e-7 relative), else
+                        // A_bar (1 / A) - 1 / A, whose error (ex2's 2^-22 over |z|) stays below
+                        // 4e-6 relative there. A = 0 gives the series' limit, dt.
                         const f2 z2 = mul2(e2, pk(kLn2, kLn2));
-                        f2 sr = fma2(z2, pk(1.f / 120.f, 1.f / 120.f), pk(1.f / 24.f, 1.f / 24.f));
-                        sr = fma2(z2, sr, pk(1.f / 6.f, 1.f / 6.f));
+                        f2 sr = fma2(z2, pk(1.f / 24.f, 1.f / 24.f), pk(1.f / 6.f, 1.f / 6.f));
                         sr = fma2(z2, sr, pk(0.5f, 0.5f));
                         sr = fma2(z2, sr, pk(1.f, 1.f));
                         float z0, z1, s0, s1, b0, b1;
                         upk(z2, z0, z1);
                         upk(mul2(dt2, sr), s0, s1);
-                        upk(mul2(fma2(ab, pk(1.f, 1.f), pk(-1.f, -1.f)), Ainv[k]), b0, b1);
-                        const f2 coef = pk(fabsf(z0) < 0.125f ? s0 : b0, fabsf(z1) < 0.125f ? s1 : b1);
+                        upk(fma2(ab, Ainv[k], nAinv[k]), b0, b1);
+                        const f2 coef = pk(fabsf(z0) < 0.0625f ? s0 : b0, fabsf(z1) < 0.0625f ? s1 : b1);
                         ub = mul2(mul2(coef, u2), bv[k]);
                     } else {
                         ub = mul2(u2, bv[k]);
@@ -352,31 +410,41 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
                 }
             }
             if constexpr (kReadout) {
-                // reduce-scatter over the LPC lanes of the channel: each round a lane keeps the
-                // half of its partial sums whose step index has its lane bit and adds the
-                // partner's; lane g ends with the full sum of step g
+                // reduce-scatter over the LPC lanes of the channel, once for steps 0 .. LPC-1 and
+                // once for LPC .. 2 LPC-1 of the supergroup: each round a lane keeps the half of
+                // its partial sums whose step index has its lane bit and adds the partner's; lane
+                // g ends with the full sums of steps g and g + LPC
 #pragma unroll
-                for (int m = LPC / 2; m >= 1; m >>= 1) {
-                    const bool upper = (g & m) != 0;
+                for (int hf = 0; hf < 2; ++hf) {
+                    float* a = acc + hf * LPC;
 #pragma unroll
-                    for (int i = 0; i < m; ++i) {
-                        const float keep = upper ? acc[i + m] : acc[i];
-                        const float send = upper ? acc[i] : acc[i + m];
-                        acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                    for (int m = LPC / 2; m >= 1; m >>= 1) {
+                        const bool upper = (g & m) != 0;
+#pragma unroll
+                        for (int i = 0; i < m; ++i) {
+                            const float keep = upper ? a[i + m] : a[i];
+                            const float send = upper ? a[i] : a[i + m];
+                            a[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                        }
                     }
                 }
-                yout[grp] = (acc[0] + cur.dx) * cur.gate;
+                yout[sg] = mul2(add2(pk(acc[0], acc[LPC]), cur.dx), cur.gate);
             }
             cur = nxt;
         }
         if constexpr (kReadout) {
 #pragma unroll
-            for (int grp = 0; grp < kT / LPC; ++grp) {
-                const int jj = rr(grp * LPC + g);
-                if constexpr (BF16)
-                    reinterpret_cast<__nv_bfloat16*>(ys)[jj * kCh + c] = __float2bfloat16_rn(yout[grp]);
-                else
-                    reinterpret_cast<float*>(ys)[jj * kCh + c] = yout[grp];
+            for (int sg = 0; sg < kNSG; ++sg) {
+                const int j0 = rr(sg * kSG + g), j1 = rr(sg * kSG + g + LPC);
+                float y0, y1;
+                upk(yout[sg], y0, y1);
+                if constexpr (BF16) {
+                    reinterpret_cast<__nv_bfloat16*>(ys)[j0 * kCh + c] = __float2bfloat16_rn(y0);
+                    reinterpret_cast<__nv_bfloat16*>(ys)[j1 * kCh + c] = __float2bfloat16_rn(y1);
+                } else {
+                    reinterpret_cast<float*>(ys)[j0 * kCh + c] = y0;
+                    reinterpret_cast<float*>(ys)[j1 * kCh + c] = y1;
+                }
             }
             fence_proxy_async_smem();
         }

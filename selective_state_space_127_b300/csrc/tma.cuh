@@ -140,4 +140,22 @@ __device__ __forceinline__ f2 mul2(f2 a, f2 b) {
     return d;
 }
 
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+    f2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ float lo_of(f2 v) {
+    float lo, hi;
+    upk(v, lo, hi);
+    return lo;
+}
+
+__device__ __forceinline__ float hi_of(f2 v) {
+    float lo, hi;
+    upk(v, lo, hi);
+    return hi;
+}
+
 }  // namespace ssm
