@@ -55,6 +55,10 @@ def parse():
     ap.add_argument("--no-conv", action="store_true", help="skip the conv1d + SiLU prologue measurements")
     ap.add_argument("--no-variants", action="store_true", help="skip the exact-ZOH and reverse measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the scan configs other than the headline")
+    ap.add_argument("--seqlen", type=int, default=0,
+                    help="shorten the headline workload to this many steps (smaller profiling captures; the "
+                         "line then names the shortened workload)")
     return ap.parse_args()
 
 
@@ -306,7 +310,7 @@ def scan_phases(w, chunk):
     return [("local pass", p1_units, p1_bytes), ("chunk carry", 0, carry_bytes), ("output pass", w.units, p2_bytes)]
 
 
-def bench_scan(k, steps, warmup, dev, rank, world, barrier, peaks, with_phases=True):
+def bench_scan(k, steps, warmup, dev, rank, world, barrier, peaks, with_phases=True, seqlen=0):
     """Time scan workload k: `warmup` untimed steps, then `steps` steps between CUDA events on
     the launching stream. With phase events each step records an event before its first
     kernel and after each kernel, so every kernel's average duration inside the timed region
@@ -316,7 +320,10 @@ def bench_scan(k, steps, warmup, dev, rank, world, barrier, peaks, with_phases=T
     from selective_state_space_127_b300.synth import SCAN_WORKLOADS, scan_workload_inputs
 
     w = SCAN_WORKLOADS[k]
-    inp = scan_workload_inputs(k, device=dev, rank=rank)
+    if seqlen:
+        import dataclasses
+        w = dataclasses.replace(w, seqlen=seqlen, name=w.name.replace(f"L{w.seqlen}", f"L{seqlen}"))
+    inp = scan_workload_inputs(k, device=dev, rank=rank, seqlen=seqlen or None)
     y = torch.empty_like(inp["x"])
     hl = torch.empty(w.batch, w.dim, w.dstate, device=dev, dtype=torch.float32)
     stream = torch.cuda.current_stream(dev)
@@ -458,7 +465,7 @@ def run_ours(args):
     # the other scan workloads first (they also bring the GPU to its working clock)
     configs = {}
     for k in (0, 1, 2):
-        if k == args.workload:
+        if k == args.workload or args.no_configs:
             continue
         r = bench_scan(k, few, 3, dev, rank, world, barrier, peaks)
         r.pop("_window")
@@ -467,8 +474,11 @@ def run_ours(args):
         configs[str(k)] = r
 
     # the headline: exactly `steps` timed steps after `warmup` untimed ones
+    head = bench_scan(args.workload, args.steps, args.warmup, dev, rank, world, barrier, peaks, seqlen=args.seqlen)
     w = SCAN_WORKLOADS[args.workload]
-    head = bench_scan(args.workload, args.steps, args.warmup, dev, rank, world, barrier, peaks)
+    if args.seqlen:
+        import dataclasses
+        w = dataclasses.replace(w, seqlen=args.seqlen, name=head["workload"])
     t_w0, t_w1 = head.pop("_window")
     clk.mark(t_w0, t_w1)
     ms = head["ms_per_step"]
@@ -618,7 +628,7 @@ def run_ours(args):
 
     if not args.no_e2e:
         # the headline workload end to end through the C ABI from pinned host buffers
-        inp = scan_workload_inputs(args.workload, device=dev, rank=rank)
+        inp = scan_workload_inputs(args.workload, device=dev, rank=rank, seqlen=args.seqlen or None)
         host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in inp.items()}
         del inp
         bufs = {}

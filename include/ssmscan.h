@@ -42,6 +42,12 @@ extern "C" {
 
 /* Bytes at the start of every workspace that hold the device status word (a uint32 at offset 0;
  * the rest is reserved). */
+
+/* The debug build of the library (libssmscan_debug.so, built with -DSSM_DEBUG_CHECKS) checks every
+ * index its kernels compute for global memory against the array it addresses; a failed check
+ * latches SSM_ERR_BOUNDS in the call's status word and skips the access. In that build every
+ * call with L > 0 needs a workspace of at least SSM_WORKSPACE_HEADER_BYTES (the *_workspace_size
+ * queries say so). Results are otherwise identical to the normal build's. */
 #define SSM_WORKSPACE_HEADER_BYTES 256
 
 #if defined(__GNUC__)
@@ -56,7 +62,9 @@ typedef enum {
     SSM_ERR_UNSUPPORTED = 2,
     SSM_ERR_CUDA = 3,
     SSM_ERR_TIMEOUT = 4,   /* a bounded device-side wait gave up (see ssm_check_status) */
-    SSM_ERR_WORKSPACE = 5  /* workspace missing, too small or misaligned */
+    SSM_ERR_WORKSPACE = 5, /* workspace missing, too small or misaligned */
+    SSM_ERR_BOUNDS = 6     /* debug build only: a kernel's index check failed and the access was
+                              skipped (see ssm_check_status) */
 } ssm_status_t;
 
 typedef enum { SSM_DTYPE_F32 = 0, SSM_DTYPE_BF16 = 1 } ssm_dtype_t;
@@ -285,7 +293,8 @@ SSMSCAN_API ssm_status_t ssd_chunk_scan_fwd(const ssd_scan_params* p, void* stre
 /* Synchronise `stream`, then return the status word in the header of `workspace` (a device
  * pointer given to earlier calls on this stream): SSM_OK, or SSM_ERR_TIMEOUT if a bounded
  * wait of a kernel that used this workspace gave up since the word was last cleared (that
- * call's outputs are then incomplete). A timeout is visible only through the workspace of
+ * call's outputs are then incomplete), or, in the debug build, SSM_ERR_BOUNDS if a kernel's
+ * index check failed. A timeout is visible only through the workspace of
  * the call that had it. workspace == NULL reads the header of the built-in scratch of
  * ssm_scan_fwd_noalloc on the current device. With `clear` != 0 the word is reset to SSM_OK
  * afterwards. Returns SSM_ERR_CUDA if the stream reports an error. */

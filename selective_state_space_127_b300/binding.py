@@ -15,9 +15,12 @@ import threading
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libssmscan.so")
+# SSMSCAN_LIBRARY selects another build of the library (e.g. the index-checking
+# libssmscan_debug.so): a path, or a file name in the package directory.
+LIB_PATH = os.path.join(_PKG, os.environ.get("SSMSCAN_LIBRARY", "libssmscan.so"))
 
-SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_WORKSPACE = range(6)
+SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_WORKSPACE, SSM_ERR_BOUNDS = \
+    range(7)
 SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
 SSM_DISC_DELTA_B, SSM_DISC_ZOH = 0, 1
 ABI_VERSION = 3
@@ -115,7 +118,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 
 def _status_name(s: int) -> str:
     return ["SSM_OK", "SSM_ERR_INVALID_ARG", "SSM_ERR_UNSUPPORTED", "SSM_ERR_CUDA", "SSM_ERR_TIMEOUT",
-            "SSM_ERR_WORKSPACE"][s] if 0 <= s <= 5 else f"status {s}"
+            "SSM_ERR_WORKSPACE", "SSM_ERR_BOUNDS"][s] if 0 <= s <= 6 else f"status {s}"
 
 
 def _check(lib, status: int):

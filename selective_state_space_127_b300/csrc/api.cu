@@ -211,6 +211,19 @@ ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
     a.status = nullptr;
     a.phase_events = p->phase_events;
     a.n_phase_events = p->n_phase_events;
+    auto ext = [](const int64_t* sizes, const int64_t* st) {
+        int64_t e = 1;
+        for (int i = 0; i < 3; ++i) e += (sizes[i] - 1) * st[i];
+        return e;
+    };
+    const int64_t act[3] = {p->batch, p->seqlen > 0 ? p->seqlen : 1, p->dim};
+    const int64_t bc[3] = {p->batch, p->seqlen > 0 ? p->seqlen : 1, p->dstate};
+    a.ext_x = ext(act, p->x_stride);
+    a.ext_delta = ext(act, p->delta_stride);
+    a.ext_z = ext(act, p->z_stride);
+    a.ext_y = ext(act, p->y_stride);
+    a.ext_B = ext(bc, p->B_stride);
+    a.ext_C = ext(bc, p->C_stride);
     return SSM_OK;
 }
 
@@ -265,10 +278,20 @@ ssm_status_t validate_conv1d(const ssm_conv1d_params* p, ssm::Conv1dArgs* out) {
 // written once (in place when h0 == h_last).
 constexpr int64_t kShortSeq = 4;
 
+// Whether every path needs the status header: in the debug build every kernel can report a
+// failed index check there.
+#ifdef SSM_DEBUG_CHECKS
+constexpr bool kStatusEverywhere = true;
+#else
+constexpr bool kStatusEverywhere = false;
+#endif
+
 // The TMA kernels wait (bounded) on their copies, so they need the status header; the split
-// sequence adds its chunk carries after it. The short-sequence and generic kernels need none.
+// sequence adds its chunk carries after it. The short-sequence and generic kernels need none
+// (except in the debug build).
 size_t scan_workspace_bytes(const ssm::ScanArgs& a) {
-    if (a.seqlen <= kShortSeq || !ssm::scan_fast_supported(a)) return 0;
+    if (a.seqlen <= kShortSeq || !ssm::scan_fast_supported(a))
+        return kStatusEverywhere && a.seqlen > 0 ? SSM_WORKSPACE_HEADER_BYTES : 0;
     return SSM_WORKSPACE_HEADER_BYTES + ssm::scan_fast_workspace_bytes(a);
 }
 
@@ -424,7 +447,7 @@ ssm_status_t ssm_causal_conv1d_fwd(const ssm_conv1d_params* p, void* stream) {
 size_t ssd_chunk_scan_workspace_size(const ssd_scan_params* p) {
     ssm::SSDArgs a;
     if (validate_ssd(p, &a) != SSM_OK) return (size_t)-1;
-    return a.seqlen > 0 && ssm::ssd_tc_supported(a) ? SSM_WORKSPACE_HEADER_BYTES : 0;
+    return a.seqlen > 0 && (kStatusEverywhere || ssm::ssd_tc_supported(a)) ? SSM_WORKSPACE_HEADER_BYTES : 0;
 }
 
 ssm_status_t ssd_chunk_scan_fwd(const ssd_scan_params* p, void* stream) {
@@ -433,7 +456,7 @@ ssm_status_t ssd_chunk_scan_fwd(const ssd_scan_params* p, void* stream) {
     if (s != SSM_OK) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
-    if (a.seqlen > 0 && ssm::ssd_tc_supported(a)) {
+    if (a.seqlen > 0 && (kStatusEverywhere || ssm::ssd_tc_supported(a))) {
         s = attach_workspace(a.workspace, a.workspace_bytes, SSM_WORKSPACE_HEADER_BYTES, &a.status);
         if (s != SSM_OK) return s;
     }
@@ -479,6 +502,7 @@ const char* ssm_status_string(ssm_status_t s) {
         case SSM_ERR_CUDA: return "SSM_ERR_CUDA";
         case SSM_ERR_TIMEOUT: return "SSM_ERR_TIMEOUT";
         case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE";
+        case SSM_ERR_BOUNDS: return "SSM_ERR_BOUNDS";
     }
     return "SSM_ERR_UNKNOWN";
 }

@@ -6,6 +6,23 @@
 
 namespace ssm {
 
+// ---------------------------------------------------------------- index checks (debug build)
+// A library compiled with -DSSM_DEBUG_CHECKS (`python -m selective_state_space_127_b300.build
+// --debug-checks` -> libssmscan_debug.so) checks every computed global-memory index of its
+// kernels against the extent of the array it addresses (TMA boxes are clipped by the hardware
+// and need no check): an index outside latches SSM_ERR_BOUNDS in the call's status word and the
+// access is skipped (a load reads zero). No trap, no fault. The normal build compiles the
+// checks out.
+#ifdef SSM_DEBUG_CHECKS
+__device__ __forceinline__ bool idx_ok(int64_t i, int64_t n, unsigned* status) {
+    if (i >= 0 && i < n) return true;
+    if (status) atomicExch(status, 6u /* SSM_ERR_BOUNDS */);
+    return false;
+}
+#else
+__device__ __forceinline__ bool idx_ok(int64_t, int64_t, unsigned*) { return true; }
+#endif
+
 constexpr float kLog2e = 1.4426950408889634f;  // log2(e)
 constexpr float kLn2 = 0.6931471805599453f;    // ln(2)
 

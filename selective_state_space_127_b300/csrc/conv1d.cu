@@ -88,11 +88,11 @@ conv1d_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CU
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         const int64_t c = c0 + e;
-        bv[e] = (c < p.dim && p.bias) ? p.bias[c] : 0.f;
+        bv[e] = (c < p.dim && p.bias && idx_ok(c, p.dim, p.status)) ? p.bias[c] : 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int k = j - (4 - p.K);
-            w4[e][j] = (c < p.dim && k >= 0) ? p.w[c * p.K + k] : 0.f;
+            w4[e][j] = (c < p.dim && k >= 0 && idx_ok(c * p.K + k, p.dim * p.K, p.status)) ? p.w[c * p.K + k] : 0.f;
         }
     }
 
@@ -142,8 +142,10 @@ conv1d_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CU
                 for (int e = 0; e < E; ++e) {
                     const int64_t c = c0 + e;
                     float v = 0.f;
-                    if (m <= p.K - 1 && c < p.dim)
-                        v = load_f32(p.x_prev, ((int64_t)b * (p.K - 1) + (p.K - 1 - m)) * p.dim + c, BF16);
+                    if (m <= p.K - 1 && c < p.dim) {
+                        const int64_t ip = ((int64_t)b * (p.K - 1) + (p.K - 1 - m)) * p.dim + c;
+                        if (idx_ok(ip, p.batch * (p.K - 1) * p.dim, p.status)) v = load_f32(p.x_prev, ip, BF16);
+                    }
                     win[3 - m][e] = v;
                 }
         } else {

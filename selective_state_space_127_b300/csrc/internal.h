@@ -40,6 +40,9 @@ struct ScanArgs {
     unsigned* status;        // the workspace header's status word (nullptr when no workspace)
     void* const* phase_events;   // cudaEvent_t handles recorded around the launches, or nullptr
     int n_phase_events;
+    // element extents (largest index + 1) of the strided views x, delta, z, y, B, C: the bounds
+    // the debug build checks computed indices against
+    int64_t ext_x, ext_delta, ext_z, ext_y, ext_B, ext_C;
 };
 
 struct Conv1dArgs {

@@ -30,13 +30,13 @@ __global__ void __launch_bounds__(kDecodeThreads) scan_decode_kernel(const ScanA
     const int n0 = 4 * g;
 
     float Av[4] = {0.f, 0.f, 0.f, 0.f}, h[4] = {0.f, 0.f, 0.f, 0.f};
-    if (active) {
+    if (active && idx_ok(d * N + n0 + 3, a.dim * N, a.status)) {
         const float4 a4 = *reinterpret_cast<const float4*>(a.A + d * N + n0);
         Av[0] = a4.x;
         Av[1] = a4.y;
         Av[2] = a4.z;
         Av[3] = a4.w;
-        if (a.h0) {
+        if (a.h0 && idx_ok((b * a.dim + d) * N + n0 + 3, a.batch * a.dim * N, a.status)) {
             const float4 h4 = *reinterpret_cast<const float4*>(a.h0 + (b * a.dim + d) * N + n0);
             h[0] = h4.x;
             h[1] = h4.y;
@@ -44,20 +44,25 @@ __global__ void __launch_bounds__(kDecodeThreads) scan_decode_kernel(const ScanA
             h[3] = h4.w;
         }
     }
-    const float Dd = (active && a.D) ? a.D[d] : 0.f;
-    const float bias = (active && a.bias) ? a.bias[d] : 0.f;
+    const float Dd = (active && a.D && idx_ok(d, a.dim, a.status)) ? a.D[d] : 0.f;
+    const float bias = (active && a.bias && idx_ok(d, a.dim, a.status)) ? a.bias[d] : 0.f;
 
     for (int64_t step = 0; step < a.seqlen; ++step) {
         const int64_t t = a.reverse ? a.seqlen - 1 - step : step;
         float xv = 0.f, dv = 0.f, zv = 0.f, Bn[4] = {0.f, 0.f, 0.f, 0.f}, Cn[4] = {0.f, 0.f, 0.f, 0.f};
         if (active) {
-            xv = load_f32(a.x, b * a.xs[0] + t * a.xs[1] + d * a.xs[2], a.io_bf16);
-            dv = load_f32(a.delta, b * a.ds[0] + t * a.ds[1] + d * a.ds[2], a.io_bf16);
-            if (a.z) zv = load_f32(a.z, b * a.zs[0] + t * a.zs[1] + d * a.zs[2], a.io_bf16);
+            const int64_t ix = b * a.xs[0] + t * a.xs[1] + d * a.xs[2];
+            const int64_t id = b * a.ds[0] + t * a.ds[1] + d * a.ds[2];
+            const int64_t iz = b * a.zs[0] + t * a.zs[1] + d * a.zs[2];
+            if (idx_ok(ix, a.ext_x, a.status)) xv = load_f32(a.x, ix, a.io_bf16);
+            if (idx_ok(id, a.ext_delta, a.status)) dv = load_f32(a.delta, id, a.io_bf16);
+            if (a.z && idx_ok(iz, a.ext_z, a.status)) zv = load_f32(a.z, iz, a.io_bf16);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                Bn[k] = load_f32(a.B, b * a.Bs[0] + t * a.Bs[1] + (n0 + k) * a.Bs[2], a.io_bf16);
-                Cn[k] = load_f32(a.C, b * a.Cs[0] + t * a.Cs[1] + (n0 + k) * a.Cs[2], a.io_bf16);
+                const int64_t ib = b * a.Bs[0] + t * a.Bs[1] + (n0 + k) * a.Bs[2];
+                const int64_t ic = b * a.Cs[0] + t * a.Cs[1] + (n0 + k) * a.Cs[2];
+                if (idx_ok(ib, a.ext_B, a.status)) Bn[k] = load_f32(a.B, ib, a.io_bf16);
+                if (idx_ok(ic, a.ext_C, a.status)) Cn[k] = load_f32(a.C, ic, a.io_bf16);
             }
         }
         float dt = dv + bias;
@@ -76,10 +81,11 @@ __global__ void __launch_bounds__(kDecodeThreads) scan_decode_kernel(const ScanA
         if (active && g == 0) {
             float out = fmaf(Dd, xv, acc);
             if (a.z) out *= silu_accurate(zv);
-            store_io(a.y, b * a.ys[0] + t * a.ys[1] + d * a.ys[2], out, a.io_bf16);
+            const int64_t iy = b * a.ys[0] + t * a.ys[1] + d * a.ys[2];
+            if (idx_ok(iy, a.ext_y, a.status)) store_io(a.y, iy, out, a.io_bf16);
         }
     }
-    if (active && a.h_last)
+    if (active && a.h_last && idx_ok((b * a.dim + d) * N + n0 + 3, a.batch * a.dim * N, a.status))
         *reinterpret_cast<float4*>(a.h_last + (b * a.dim + d) * N + n0) = make_float4(h[0], h[1], h[2], h[3]);
 }
 

@@ -10,7 +10,7 @@
 // channel, lane g keeping the fp32 states n in [g S, g S + S), S = N / LPC, in registers.
 //
 // Data movement. TMA (3-D tensor maps over (D or N, L, b)) streams 32-step tiles of x,
-// delta, z, B and C into a 3-deep shared-memory ring guarded by mbarriers; y tiles leave
+// delta, z, B and C into a 2-deep shared-memory ring guarded by mbarriers; y tiles leave
 // through TMA stores from a double buffer. B and C tiles are widened to fp32 once per tile
 // by the CTA, so lanes then read their states' values with 8- or 16-byte loads.
 //
@@ -57,19 +57,22 @@ namespace {
 // where slot c + 1 holds local_c (pass 1), and stores H_c into slot c: the initial state of
 // every chunk, chunk 0's being a copy of h0 (so that h0 may alias h_last).
 __global__ void scan_carry_kernel(float* carry, const float* sumdt, const float* A, const float* h0,
-                                  int64_t batch, int64_t dim, int N, int nsteps) {
+                                  int64_t batch, int64_t dim, int N, int nsteps, unsigned* status) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t total = batch * dim * N;
     if (i >= total) return;
     const int64_t bd = i / N;
     const int n = (int)(i % N);
     const int64_t d = bd % dim;
-    const float a = A[d * N + n];
+    const float a = idx_ok(d * N + n, dim * N, status) ? A[d * N + n] : 0.f;
     float H = h0 ? h0[i] : 0.f;
     carry[i] = H;
     for (int c = 0; c < nsteps; ++c) {
         const int64_t o = (int64_t)(c + 1) * total + i;
-        H = fmaf(expf(a * sumdt[(int64_t)c * batch * dim + bd]), H, carry[o]);
+        const int64_t os = (int64_t)c * batch * dim + bd;
+        if (!idx_ok(o, (int64_t)(nsteps + 1) * total, status) || !idx_ok(os, (int64_t)nsteps * batch * dim, status))
+            break;
+        H = fmaf(expf(a * sumdt[os]), H, carry[o]);
         carry[o] = H;
     }
 }
@@ -203,7 +206,7 @@ cudaError_t launch_scan_fast(const ScanArgs& a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         const int64_t total = a.batch * a.dim * a.dstate;
         scan_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(fp.carry, fp.sumdt, a.A, a.h0, a.batch,
-                                                                          a.dim, a.dstate, nch - 1);
+                                                                          a.dim, a.dstate, nch - 1, a.status);
         note_launches(1);
         e = cudaGetLastError();
         if (e == cudaSuccess) e = record_phase(a, 2, false, st);

@@ -38,30 +38,38 @@ scan_generic_kernel(const ScanArgs a) {
     for (int s = 0; s < S; ++s) {
         const int n = n0 + s;
         const bool ok = active && n < N;
-        Araw[s] = ok ? a.A[d * N + n] : 0.f;
+        Araw[s] = ok && idx_ok(d * N + n, a.dim * N, a.status) ? a.A[d * N + n] : 0.f;
         A2[s] = Araw[s] * kLog2e;
-        h[s] = (ok && a.h0) ? a.h0[(b * a.dim + d) * N + n] : 0.f;
+        h[s] = (ok && a.h0 && idx_ok((b * a.dim + d) * N + n, a.batch * a.dim * N, a.status))
+                   ? a.h0[(b * a.dim + d) * N + n]
+                   : 0.f;
     }
-    const float Dd = (active && a.D) ? a.D[d] : 0.f;
-    const float bias = (active && a.bias) ? a.bias[d] : 0.f;
+    const float Dd = (active && a.D && idx_ok(d, a.dim, a.status)) ? a.D[d] : 0.f;
+    const float bias = (active && a.bias && idx_ok(d, a.dim, a.status)) ? a.bias[d] : 0.f;
     // conv prologue: taps right-aligned into cw[0..3] (cw[3] multiplies x_t), win = x_{t-3..t-1}
     float cw[4] = {0.f, 0.f, 0.f, 0.f}, cb = 0.f, win[3] = {0.f, 0.f, 0.f};
     if (a.conv_w && active) {
         const int K = a.conv_k;
-        for (int j = 4 - K; j < 4; ++j) cw[j] = a.conv_w[d * K + j - (4 - K)];
+        for (int j = 4 - K; j < 4; ++j)
+            if (idx_ok(d * K + j - (4 - K), a.dim * K, a.status)) cw[j] = a.conv_w[d * K + j - (4 - K)];
         cb = a.conv_b ? a.conv_b[d] : 0.f;
         if (a.conv_prev)
-            for (int m = 1; m < K; ++m)   // x_{-m} = x_prev[b, K-1-m]
-                win[3 - m] = load_f32(a.conv_prev, (b * (K - 1) + (K - 1 - m)) * a.dim + d, a.io_bf16);
+            for (int m = 1; m < K; ++m) {   // x_{-m} = x_prev[b, K-1-m]
+                const int64_t i = (b * (K - 1) + (K - 1 - m)) * a.dim + d;
+                if (idx_ok(i, a.batch * (K - 1) * a.dim, a.status)) win[3 - m] = load_f32(a.conv_prev, i, a.io_bf16);
+            }
     }
 
     for (int64_t step = 0; step < a.seqlen; ++step) {
         const int64_t t = a.reverse ? a.seqlen - 1 - step : step;
         float xv = 0.f, dv = 0.f, zv = 0.f;
         if (active) {
-            xv = load_f32(a.x, b * a.xs[0] + t * a.xs[1] + d * a.xs[2], a.io_bf16);
-            dv = load_f32(a.delta, b * a.ds[0] + t * a.ds[1] + d * a.ds[2], a.io_bf16);
-            if (a.z) zv = load_f32(a.z, b * a.zs[0] + t * a.zs[1] + d * a.zs[2], a.io_bf16);
+            const int64_t ix = b * a.xs[0] + t * a.xs[1] + d * a.xs[2];
+            const int64_t id = b * a.ds[0] + t * a.ds[1] + d * a.ds[2];
+            const int64_t iz = b * a.zs[0] + t * a.zs[1] + d * a.zs[2];
+            if (idx_ok(ix, a.ext_x, a.status)) xv = load_f32(a.x, ix, a.io_bf16);
+            if (idx_ok(id, a.ext_delta, a.status)) dv = load_f32(a.delta, id, a.io_bf16);
+            if (a.z && idx_ok(iz, a.ext_z, a.status)) zv = load_f32(a.z, iz, a.io_bf16);
         }
         if (a.conv_w) {
             const float v = fmaf(cw[3], xv, fmaf(cw[2], win[2], fmaf(cw[1], win[1], fmaf(cw[0], win[0], cb))));
@@ -78,8 +86,10 @@ scan_generic_kernel(const ScanArgs a) {
         for (int s = 0; s < S; ++s) {
             const int n = n0 + s;
             if (active && n < N) {
-                const float Bn = load_f32(a.B, b * a.Bs[0] + t * a.Bs[1] + n * a.Bs[2], a.io_bf16);
-                const float Cn = load_f32(a.C, b * a.Cs[0] + t * a.Cs[1] + n * a.Cs[2], a.io_bf16);
+                const int64_t ib = b * a.Bs[0] + t * a.Bs[1] + n * a.Bs[2];
+                const int64_t ic = b * a.Cs[0] + t * a.Cs[1] + n * a.Cs[2];
+                const float Bn = idx_ok(ib, a.ext_B, a.status) ? load_f32(a.B, ib, a.io_bf16) : 0.f;
+                const float Cn = idx_ok(ic, a.ext_C, a.status) ? load_f32(a.C, ic, a.io_bf16) : 0.f;
                 const float abar = ex2_approx(dt * A2[s]);
                 float bx;
                 if (a.zoh && Araw[s] != 0.f)
@@ -95,14 +105,16 @@ scan_generic_kernel(const ScanArgs a) {
         if (active && g == 0) {
             float out = fmaf(Dd, xv, acc);
             if (a.z) out *= silu_accurate(zv);
-            store_io(a.y, b * a.ys[0] + t * a.ys[1] + d * a.ys[2], out, a.io_bf16);
+            const int64_t iy = b * a.ys[0] + t * a.ys[1] + d * a.ys[2];
+            if (idx_ok(iy, a.ext_y, a.status)) store_io(a.y, iy, out, a.io_bf16);
         }
     }
     if (active && a.h_last) {
 #pragma unroll
         for (int s = 0; s < S; ++s) {
             const int n = n0 + s;
-            if (n < N) a.h_last[(b * a.dim + d) * N + n] = h[s];
+            if (n < N && idx_ok((b * a.dim + d) * N + n, a.batch * a.dim * N, a.status))
+                a.h_last[(b * a.dim + d) * N + n] = h[s];
         }
     }
 }

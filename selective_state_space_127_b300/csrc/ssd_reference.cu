@@ -49,10 +49,14 @@ ssd_reference_kernel(const SSDArgs a) {
 
     float S[ROWS];
     const int rows = (N + J - 1) / J;
+    // extents for the index checks of the debug build
+    const int64_t n_state = a.batch * a.nheads * N * P, n_act = a.batch * a.seqlen * a.nheads * P;
+    const int64_t n_bc = a.batch * a.seqlen * a.ngroups * N, n_dt = a.batch * a.seqlen * a.nheads;
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
         const int n = j * rows + r;
-        S[r] = (active && r < rows && n < N && a.h0) ? a.h0[((b * a.nheads + hh) * N + n) * P + p] : 0.f;
+        const int64_t is = ((b * a.nheads + hh) * N + n) * P + p;
+        S[r] = (active && r < rows && n < N && a.h0 && idx_ok(is, n_state, a.status)) ? a.h0[is] : 0.f;
     }
     const float Ah = a.A[hh] * kLog2e;
     const float bias = a.bias ? a.bias[hh] : 0.f;
@@ -64,17 +68,20 @@ ssd_reference_kernel(const SSDArgs a) {
         for (int i = tid; i < nt * N; i += kRefThreads) {
             const int tt = i / N, n = i % N;
             const int64_t row = (b * a.seqlen + t0 + tt) * a.ngroups + grp;
-            sB[tt * N + n] = load_f32(a.B, row * N + n, a.io_bf16);
-            sC[tt * N + n] = load_f32(a.C, row * N + n, a.io_bf16);
+            const bool okb = idx_ok(row * N + n, n_bc, a.status);
+            sB[tt * N + n] = okb ? load_f32(a.B, row * N + n, a.io_bf16) : 0.f;
+            sC[tt * N + n] = okb ? load_f32(a.C, row * N + n, a.io_bf16) : 0.f;
         }
         for (int i = tid; i < nt * P; i += kRefThreads) {
             const int tt = i / P, q = i % P;
-            sx[tt * P + q] = load_f32(a.x, ((b * a.seqlen + t0 + tt) * a.nheads + hh) * P + q, a.io_bf16);
+            const int64_t ix = ((b * a.seqlen + t0 + tt) * a.nheads + hh) * P + q;
+            sx[tt * P + q] = idx_ok(ix, n_act, a.status) ? load_f32(a.x, ix, a.io_bf16) : 0.f;
         }
         if (tid < kT) {
             float dt = 0.f;
-            if (tid < nt) {
-                dt = load_f32(a.delta, (b * a.seqlen + t0 + tid) * a.nheads + hh, a.io_bf16) + bias;
+            const int64_t id = (b * a.seqlen + t0 + tid) * a.nheads + hh;
+            if (tid < nt && idx_ok(id, n_dt, a.status)) {
+                dt = load_f32(a.delta, id, a.io_bf16) + bias;
                 if (a.softplus) dt = softplus_accurate(dt);
             }
             sdt[tid] = dt;
@@ -126,6 +133,7 @@ ssd_reference_kernel(const SSDArgs a) {
             for (int g = 0; g < J; ++g) out += part[(g * kT + tt) * P + q];
             out = fmaf(Dh, sx[tt * P + q], out);
             const int64_t xi = ((b * a.seqlen + t0 + tt) * a.nheads + hh) * P + q;
+            if (!idx_ok(xi, n_act, a.status)) continue;
             if (a.z) out *= silu_accurate(load_f32(a.z, xi, a.io_bf16));
             store_io(a.y, xi, out, a.io_bf16);
         }
@@ -135,7 +143,8 @@ ssd_reference_kernel(const SSDArgs a) {
 #pragma unroll
         for (int r = 0; r < ROWS; ++r) {
             const int n = j * rows + r;
-            if (r < rows && n < N) a.h_last[((b * a.nheads + hh) * N + n) * P + p] = S[r];
+            const int64_t is = ((b * a.nheads + hh) * N + n) * P + p;
+            if (r < rows && n < N && idx_ok(is, n_state, a.status)) a.h_last[is] = S[r];
         }
     }
 }

@@ -344,7 +344,8 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
         const uintptr_t dl_hi = 2;
         auto load_delta = [&](int j) {
             const int64_t tt = (int64_t)j * kQ + row;
-            if (half == 0 && j < nblk && tt < L) {
+            if (half == 0 && j < nblk && tt < L &&
+                idx_ok(((int64_t)b * L + tt) * H + h, (int64_t)gridDim.y * L * H, p.status)) {
                 const uintptr_t a = reinterpret_cast<uintptr_t>(delta + ((int64_t)b * L + tt) * H + h);
                 cp_async4(sm + kSmDl + (j & 1) * kQ * 4 + row * 4, reinterpret_cast<const void*>(a & ~(uintptr_t)3));
             }
@@ -399,7 +400,9 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
         // initial state: row `row`, columns [32 half, +32) in registers, bf16 copy in sS
         float S[kP / 2];
         {
-            const float* src = p.h0 ? p.h0 + (((int64_t)b * H + h) * kN + row) * kP + 32 * half : nullptr;
+            const int64_t is = (((int64_t)b * H + h) * kN + row) * kP + 32 * half;
+            const float* src =
+                p.h0 && idx_ok(is + 31, (int64_t)gridDim.y * H * kN * kP, p.status) ? p.h0 + is : nullptr;
 #pragma unroll
             for (int i = 0; i < kP / 2; i += 4) {
                 const float4 v = src ? *reinterpret_cast<const float4*>(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -431,10 +434,12 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
                 const int64_t t = (int64_t)jj * kQ + row;
                 const float e_t = arr(sj, 2)[row];
                 const float e_last = red[4 + sj];
-                const __nv_bfloat16* xrow = p.D && t < L ? static_cast<const __nv_bfloat16*>(p.x) +
+                const int64_t irow = (((int64_t)b * L + t) * H + h) * kP + 32 * half;
+                const bool row_ok = t < L && idx_ok(irow + 31, (int64_t)gridDim.y * L * H * kP, p.status);
+                const __nv_bfloat16* xrow = p.D && row_ok ? static_cast<const __nv_bfloat16*>(p.x) +
                                                                (((int64_t)b * L + t) * H + h) * kP + 32 * half
                                                          : nullptr;
-                const __nv_bfloat16* zrow = p.z && t < L ? static_cast<const __nv_bfloat16*>(p.z) +
+                const __nv_bfloat16* zrow = p.z && row_ok ? static_cast<const __nv_bfloat16*>(p.z) +
                                                                (((int64_t)b * L + t) * H + h) * kP + 32 * half
                                                          : nullptr;
                 unsigned char* ys = sm + kSmX + (jj % 3) * kAtom;
@@ -593,7 +598,9 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
         }
         if (ok && nblk > 0) ok = epilogue(nblk - 1, true);
         cp_async_wait<0>();   // no copy may land after the block has left
-        if (ok && p.h_last) {
+        if (ok && p.h_last &&
+            idx_ok((((int64_t)b * H + h) * kN + row) * kP + 32 * half + 31, (int64_t)gridDim.y * H * kN * kP,
+                   p.status)) {
             float* dst = p.h_last + (((int64_t)b * H + h) * kN + row) * kP + 32 * half;
 #pragma unroll
             for (int i = 0; i < kP / 2; i += 4)

@@ -44,7 +44,7 @@ def test_library_needs_no_cuda_shared_runtime():
 
 def test_abi_version_and_status_strings(lib):
     assert lib.ssm_abi_version() == binding.ABI_VERSION
-    for code in range(6):
+    for code in range(7):
         assert lib.ssm_status_string(code).decode() == binding._status_name(code)
 
 
@@ -249,3 +249,14 @@ def test_invalid_conv1d_args_are_rejected_before_launch(lib, field, value, statu
     assert lib.ssm_causal_conv1d_fwd(ctypes.byref(p), None) == status
     assert lib.ssm_last_error().decode() != ""
     assert lib.ssm_causal_conv1d_fwd(None, None) == binding.SSM_ERR_INVALID_ARG
+
+
+def test_debug_build_exports_the_same_symbols():
+    from selective_state_space_127_b300.build import DEBUG_LIB_PATH, build as build_lib
+    build_lib(debug_checks=True)
+    out = subprocess.check_output(["nm", "-D", "--defined-only", DEBUG_LIB_PATH]).decode()
+    exported = set(re.findall(r" T (\w+)$", out, flags=re.M))
+    assert set(_declared_functions()) <= exported
+    lib = ctypes.CDLL(DEBUG_LIB_PATH)
+    lib.ssm_status_string.restype = ctypes.c_char_p
+    assert lib.ssm_status_string(binding.SSM_ERR_BOUNDS).decode() == "SSM_ERR_BOUNDS"
