@@ -21,7 +21,9 @@
 // blocks; the result does not depend on the chunk length beyond rounding.
 //
 // Pipeline. A control warp issues the TMA loads, the MMAs and the y stores; eight math warps
-// (two per TMEM lane quarter, splitting the columns) run the block scan of dt A, the mask,
+// (two per TMEM lane quarter, each taking the same half of every 32-column chunk of the mask,
+// so both carry the same mix of factored, diagonal and zero columns) run the block scan of dt A,
+// the mask,
 // the scaled copy w o X and the epilogue. Below the diagonal the mask's decay is factored per
 // 32-step chunk, exp(cum_t - cum_s) = exp(cum_t - cum_ref) exp(cum_ref - cum_s) with cum_ref
 // the chunk's last step (both factors <= 1), so those elements need no exponential.
@@ -515,16 +517,19 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
             if (okw && j > 0) okw = wait_warp(mma2_done, (j - 1) & 1);
             tc::fence_after_sync();
             if (okw) {
-                // ---- mask: M[t, s'] = G[t, s'] exp(cum_t - cum_s') dt_s' for s' <= t; warp
-                // (quarter, half) takes the 32-column chunks half and half + 2 of its rows
+                // ---- mask: M[t, s'] = G[t, s'] exp(cum_t - cum_s') dt_s' for s' <= t. Warp
+                // (quarter, half) takes the 16-column half `half` of each 32-column chunk kc of
+                // its rows: below the diagonal chunk (kc < quarter) a factored decay, on it one
+                // exponential per element, above it zeros; both warps of a quarter get the same
+                // mix of work
                 const float cs_t = cs[row];
 #pragma unroll
-                for (int ic = 0; ic < 2; ++ic) {
-                    const int kc = half + 2 * ic;
-                    uint32_t packed[16];
+                for (int kc = 0; kc < 4; ++kc) {
+                    const int c0 = 32 * kc + 16 * half;   // first column of this half-chunk
+                    uint32_t packed[8];
                     if (kc <= quarter) {
-                        uint32_t r[32];
-                        tc::ld32(lane_base + kColG + 128 * s + 32 * kc, r);
+                        uint32_t r[16];
+                        tc::ld16(lane_base + kColG + 128 * s + c0, r);
                         tc::wait_ld();
                         if (kc < quarter) {
                             // below the diagonal: exp(cum_t - cum_s) dt_s = f_t v_s with
@@ -532,8 +537,8 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
                             const float f = ex2_approx(cs_t - cs[32 * kc + 31]);
                             const f2 f2v = pk(f, f);
 #pragma unroll
-                            for (int i = 0; i < 32; i += 4) {
-                                const ulonglong2 v4 = *reinterpret_cast<const ulonglong2*>(vs + 32 * kc + i);
+                            for (int i = 0; i < 16; i += 4) {
+                                const ulonglong2 v4 = *reinterpret_cast<const ulonglong2*>(vs + c0 + i);
                                 float m0, m1, m2, m3;
                                 upk(mul2(mul2(pk(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), v4.x), f2v), m0, m1);
                                 upk(mul2(mul2(pk(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])), v4.y), f2v), m2,
@@ -543,26 +548,27 @@ ssd_tc_kernel(const __grid_constant__ CUtensorMap mX, const __grid_constant__ CU
                             }
                         } else {
                             // the diagonal chunk: s <= t, exp(cum_t - cum_s) directly
+                            const int lim = lane - 16 * half;   // columns i <= lim are at or below t
 #pragma unroll
-                            for (int i = 0; i < 32; i += 4) {
-                                const float4 c4 = *reinterpret_cast<const float4*>(cs + 32 * kc + i);
-                                const float4 d4 = *reinterpret_cast<const float4*>(dts + 32 * kc + i);
-                                const float m0 = i <= lane ? __uint_as_float(r[i]) * d4.x * ex2_approx(cs_t - c4.x) : 0.f;
+                            for (int i = 0; i < 16; i += 4) {
+                                const float4 c4 = *reinterpret_cast<const float4*>(cs + c0 + i);
+                                const float4 d4 = *reinterpret_cast<const float4*>(dts + c0 + i);
+                                const float m0 = i <= lim ? __uint_as_float(r[i]) * d4.x * ex2_approx(cs_t - c4.x) : 0.f;
                                 const float m1 =
-                                    i + 1 <= lane ? __uint_as_float(r[i + 1]) * d4.y * ex2_approx(cs_t - c4.y) : 0.f;
+                                    i + 1 <= lim ? __uint_as_float(r[i + 1]) * d4.y * ex2_approx(cs_t - c4.y) : 0.f;
                                 const float m2 =
-                                    i + 2 <= lane ? __uint_as_float(r[i + 2]) * d4.z * ex2_approx(cs_t - c4.z) : 0.f;
+                                    i + 2 <= lim ? __uint_as_float(r[i + 2]) * d4.z * ex2_approx(cs_t - c4.z) : 0.f;
                                 const float m3 =
-                                    i + 3 <= lane ? __uint_as_float(r[i + 3]) * d4.w * ex2_approx(cs_t - c4.w) : 0.f;
+                                    i + 3 <= lim ? __uint_as_float(r[i + 3]) * d4.w * ex2_approx(cs_t - c4.w) : 0.f;
                                 packed[i / 2] = tc::pack_bf16(m0, m1);
                                 packed[i / 2 + 1] = tc::pack_bf16(m2, m3);
                             }
                         }
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) packed[i] = 0u;
+                        for (int i = 0; i < 8; ++i) packed[i] = 0u;
                     }
-                    tc::st16(lane_base + kColM + 16 * kc, packed);
+                    tc::st8(lane_base + kColM + c0 / 2, packed);
                 }
                 // ---- w o X_j: thread tid takes row tid / 2, chunks 4 (tid & 1) .. + 3, walked so
                 // that the eight lanes of a shared-memory phase hit eight bank groups
