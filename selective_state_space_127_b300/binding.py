@@ -425,21 +425,34 @@ _PER_ROW = ("x", "delta", "z", "B", "C")
 
 
 def ssm_scan_fwd_host(inputs: dict, device="cuda", stream=None, dev_buffers: dict | None = None, slices=None,
-                      **kw):
+                      segments=None, **kw):
     """End-to-end call for pinned host buffers: copy the inputs to the device, run
     ssm_scan_fwd, copy y and h_last back into pinned host tensors, synchronise.
 
-    Batch rows are independent, so the rows are split into ``slices`` groups (default
-    min(batch, 4)) whose host-to-device copy, scan and device-to-host copy run on three
-    streams (copy in, compute, copy out) and overlap across groups. ``dev_buffers`` (a
-    dict) keeps the device tensors, the pinned outputs and the streams between calls.
-    Returns (y_host, h_last_host)."""
+    The work is cut into pieces whose host-to-device copy, scan and device-to-host copy run on
+    three streams (copy in, compute, copy out), so that the copies of one piece overlap the scan
+    and the copies of its neighbours. With at least ``slices`` (default 4) batch rows the pieces
+    are groups of rows, which are independent. With fewer rows the pieces are ``segments``
+    (default 8) stretches of the sequence, scanned in order: each stretch starts from the state
+    the previous one left in the device copy of h_last (the call reads h0 before it writes
+    h_last, so the two may be one buffer), and with the conv prologue it takes the K-1 raw inputs
+    before it from the device copy of x. ``dev_buffers`` (a dict) keeps the device tensors, the
+    pinned outputs and the streams between calls. Returns (y_host, h_last_host)."""
     dev = torch.device(device)
     cache = dev_buffers if dev_buffers is not None else {}
     x = inputs["x"]
-    b = x.shape[0]
-    nsl = max(1, min(b, slices or 4))
-    bounds = [(i * b // nsl, (i + 1) * b // nsl) for i in range(nsl)]
+    b, L = x.shape[0], x.shape[1]
+    nsl = slices or 4
+    if b >= nsl or L == 0:
+        rows = [(i * b // nsl, (i + 1) * b // nsl) for i in range(min(b, nsl))] or [(0, b)]
+        pieces = [((r0, r1), (0, L)) for r0, r1 in rows]
+    else:
+        nseg = max(1, min(segments or 8, L // 64))
+        cuts = [((i * L // nseg) // 64) * 64 for i in range(nseg)] + [L]   # 64-step aligned starts
+        segs = [(cuts[i], cuts[i + 1]) for i in range(nseg) if cuts[i + 1] > cuts[i]]
+        if kw.get("reverse"):
+            segs = segs[::-1]
+        pieces = [((0, b), sg) for sg in segs]
     if "_streams" not in cache:
         cache["_streams"] = tuple(torch.cuda.Stream(device=dev) for _ in range(3))
     s_in, s_comp, s_out = cache["_streams"]
@@ -465,31 +478,57 @@ def ssm_scan_fwd_host(inputs: dict, device="cuda", stream=None, dev_buffers: dic
     if hl_host is None or hl_host.shape != hl_dev.shape:
         hl_host = torch.empty(hl_dev.shape, dtype=torch.float32, pin_memory=True)
         cache["_h_last_host"] = hl_host
+    seq_split = len(pieces) > 1 and pieces[0][0] == (0, b)
     with torch.cuda.stream(s_in):
-        for k, v in inputs.items():        # per-channel inputs: all at once
-            if v is not None and k not in _PER_ROW and k != "h0":
+        for k, v in inputs.items():        # per-channel inputs and h0: all at once
+            if v is not None and (k not in _PER_ROW + ("h0",) or (k == "h0" and seq_split)):
                 d[k].copy_(v, non_blocking=True)
-    for r0, r1 in bounds:
+    ckw = {k: v for k, v in kw.items() if k not in ("workspace", "conv_x_prev")}
+    conv_w = d["conv_weight"] if d.get("conv_weight") is not None else kw.get("conv_weight")
+    xprev0 = d["conv_x_prev"] if d.get("conv_x_prev") is not None else kw.get("conv_x_prev")
+    for i, ((r0, r1), (s0, s1)) in enumerate(pieces):
         with torch.cuda.stream(s_in):
-            for k in _PER_ROW + ("h0",):
-                if inputs.get(k) is not None:
+            for k in _PER_ROW:
+                if inputs.get(k) is None:
+                    continue
+                if s0 == 0 and s1 == L:
                     d[k][r0:r1].copy_(inputs[k][r0:r1], non_blocking=True)
+                else:                       # one contiguous stretch per row
+                    for r in range(r0, r1):
+                        d[k][r, s0:s1].copy_(inputs[k][r, s0:s1], non_blocking=True)
+            if not seq_split and inputs.get("h0") is not None:
+                d["h0"][r0:r1].copy_(inputs["h0"][r0:r1], non_blocking=True)
         s_comp.wait_stream(s_in)
-        sl = {k: (v[r0:r1] if k in _PER_ROW else v) for k, v in d.items() if k != "h0"}
-        h0 = d["h0"][r0:r1] if d.get("h0") is not None else None
-        ckw = {k: v for k, v in kw.items() if k != "workspace"}
+        sl = {k: (v[r0:r1, s0:s1] if k in _PER_ROW else v) for k, v in d.items() if k not in ("h0", "conv_x_prev")}
+        if seq_split:
+            h0 = (d["h0"] if d.get("h0") is not None else None) if i == 0 else hl_dev
+        else:
+            h0 = d["h0"][r0:r1] if d.get("h0") is not None else None
+        xprev = xprev0[r0:r1] if xprev0 is not None else None
+        if conv_w is not None and s0 > 0:   # the raw inputs before this stretch are on the device
+            K = conv_w.shape[-1]
+            with torch.cuda.stream(s_comp):
+                xprev = d["x"][r0:r1, s0 - (K - 1):s0].contiguous()
         need = scan_workspace_size(**sl, h0=h0, **ckw)
         ws = cache.get("_workspace")
         if need > 0 and (ws is None or ws.numel() < need):
             with torch.cuda.stream(s_comp):
                 ws = new_workspace(need, dev)
             cache["_workspace"] = ws
-        ssm_scan_fwd(**sl, h0=h0, out=y_dev[r0:r1], h_last=hl_dev[r0:r1], stream=s_comp,
-                     workspace=ws if need > 0 else None, **ckw)
+        ssm_scan_fwd(**sl, h0=h0, out=y_dev[r0:r1, s0:s1], h_last=hl_dev[r0:r1], stream=s_comp,
+                     workspace=ws if need > 0 else None, conv_x_prev=xprev, **ckw)
         s_out.wait_stream(s_comp)
         with torch.cuda.stream(s_out):
-            y_host[r0:r1].copy_(y_dev[r0:r1], non_blocking=True)
-            hl_host[r0:r1].copy_(hl_dev[r0:r1], non_blocking=True)
+            if s0 == 0 and s1 == L:
+                y_host[r0:r1].copy_(y_dev[r0:r1], non_blocking=True)
+            else:
+                for r in range(r0, r1):
+                    y_host[r, s0:s1].copy_(y_dev[r, s0:s1], non_blocking=True)
+            if not seq_split:
+                hl_host[r0:r1].copy_(hl_dev[r0:r1], non_blocking=True)
+    if seq_split:
+        with torch.cuda.stream(s_out):
+            hl_host.copy_(hl_dev, non_blocking=True)
     s_out.synchronize()
     return y_host, hl_host
 

@@ -238,6 +238,33 @@ def test_host_entry_point_pipelines_rows_and_matches_device_call(cuda_dev, slice
         assert torch.equal(h, h_ref.cpu())
 
 
+@pytest.mark.parametrize("segments,reverse,conv,batch", [(1, False, False, 1), (3, False, False, 1),
+                                                        (8, False, False, 2), (5, True, False, 1),
+                                                        (4, False, True, 1), (6, False, True, 3)])
+def test_host_entry_point_pipelines_sequence_stretches(cuda_dev, segments, reverse, conv, batch):
+    """With fewer rows than slices, ssm_scan_fwd_host cuts the sequence into stretches scanned
+    in order, each from the state the previous one left (and, with the conv prologue, the raw
+    inputs before it). With one chunk per call the arithmetic of every step is that of the
+    single device call, so the results are identical."""
+    L, Dm = 1000, 64
+    inp = make_scan_inputs(batch, L, Dm, 16, "bf16", seed=55, d_skip="normal", gate=True)
+    gen = torch.Generator().manual_seed(56)
+    inp["h0"] = torch.randn(batch, Dm, 16, generator=gen)
+    kw = dict(chunk_len=1024, reverse=reverse)
+    if conv:
+        inp["conv_weight"] = torch.randn(Dm, 4, generator=gen) * 0.5
+        inp["conv_bias"] = torch.randn(Dm, generator=gen) * 0.1
+        inp["conv_x_prev"] = torch.randn(batch, 3, Dm, generator=gen).to(torch.bfloat16)
+    host = {k: (v.pin_memory() if v is not None else None) for k, v in inp.items()}
+    y_ref, h_ref = ssm_scan_fwd(**_to(cuda_dev, inp), **kw)
+    torch.cuda.synchronize()
+    cache = {}
+    for _ in range(2):
+        y, h = binding.ssm_scan_fwd_host(host, device=cuda_dev, dev_buffers=cache, segments=segments, **kw)
+        assert torch.equal(y, y_ref.cpu())
+        assert torch.equal(h, h_ref.cpu())
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_decode_steps_advance_the_state_in_place(cuda_dev, dt):
     """Single-token recurrent inference: T calls with L = 1 and h0 = h_last = one state buffer
