@@ -78,26 +78,25 @@ __device__ __forceinline__ float ld_io(const void* base, int i, bool bf16) {
     return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]) : static_cast<const float*>(base)[i];
 }
 
+// log1p(e) / e on e in [0, 1] as a degree-7 polynomial in e, highest power first: the
+// least-squares fit on 4000 Chebyshev nodes of [0, 1], rounded to fp32. Evaluated by Horner's
+// rule in fp32 (e q(e) against log1p(e)) its relative error stays below 4e-7 over the interval,
+// and it holds that relative accuracy as e -> 0, where log(1 + e) itself would cancel.
+__device__ constexpr float kLog1pPoly[8] = {-0.008574675768613815f, 0.044214192777872086f, -0.10785368084907532f,
+                                            0.17757023870944977f,   -0.2449961155653f,     0.3327617645263672f,
+                                            -0.49997448921203613f,  0.9999998211860657f};
+
 // softplus(v) = log(1 + e^v) of both halves of a pair, without a branch: max(v, 0) + log1p(e)
-// with e = e^-|v| in (0, 1] from the SFU, and log1p(e) = 2 atanh(s), s = e / (2 + e) in
-// (0, 1/3], summed as 2 s (1 + s^2/3 + s^4/5 + ... + s^12/13): the first omitted term, s^15/15,
-// is below 1.5e-8 relative, and the series keeps full relative accuracy for the small steps
-// (softplus near e^v) where log(1 + e) itself would cancel.
+// with e = e^-|v| in (0, 1] from the SFU and log1p(e) = e q(e) from the polynomial above (no
+// reciprocal, so no second SFU operation).
 __device__ __forceinline__ f2 softplus2(f2 v) {
     float v0, v1;
     upk(v, v0, v1);
     const f2 e = pk(ex2_approx(-fabsf(v0) * kLog2e), ex2_approx(-fabsf(v1) * kLog2e));
-    float d0, d1;
-    upk(add2(e, pk(2.f, 2.f)), d0, d1);
-    const f2 sv = mul2(e, pk(rcp_approx(d0), rcp_approx(d1)));
-    const f2 w = mul2(sv, sv);
-    f2 q = fma2(w, pk(2.f / 13.f, 2.f / 13.f), pk(2.f / 11.f, 2.f / 11.f));
-    q = fma2(w, q, pk(2.f / 9.f, 2.f / 9.f));
-    q = fma2(w, q, pk(2.f / 7.f, 2.f / 7.f));
-    q = fma2(w, q, pk(2.f / 5.f, 2.f / 5.f));
-    q = fma2(w, q, pk(2.f / 3.f, 2.f / 3.f));
-    q = fma2(w, q, pk(2.f, 2.f));
-    return add2(mul2(sv, q), pk(fmaxf(v0, 0.f), fmaxf(v1, 0.f)));
+    f2 q = pk(kLog1pPoly[0], kLog1pPoly[0]);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) q = fma2(e, q, pk(kLog1pPoly[i], kLog1pPoly[i]));
+    return fma2(e, q, pk(fmaxf(v0, 0.f), fmaxf(v1, 0.f)));
 }
 
 // silu(z) = z / (1 + e^-z) of both halves of a pair (SFU ex2 and rcp).
