@@ -319,16 +319,17 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         // B (and C) of the tile widened to fp32
         float* bcf = reinterpret_cast<float*>(smem + Lay::kBCf);
         if constexpr (BF16) {
-            const uint4* src = reinterpret_cast<const uint4*>(st + Lay::kOffB);
-            constexpr int kChunks = (kReadout ? 2 : 1) * kT * N / 8;
+            // four values per lane and round: consecutive lanes read consecutive 8 bytes and
+            // write consecutive 16 bytes, so the stores hit no bank twice (32-byte strides per
+            // lane made them two-way conflicted)
+            const uint2* src = reinterpret_cast<const uint2*>(st + Lay::kOffB);
+            constexpr int kQuads = (kReadout ? 2 : 1) * kT * N / 4;
 #pragma unroll
-            for (int i = tid; i < kChunks; i += kThreads) {
-                const uint4 v = src[i];
-                float4* dst = reinterpret_cast<float4*>(bcf + i * 8);
-                dst[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
-                                     __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
-                dst[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u),
-                                     __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+            for (int i = tid; i < kQuads; i += kThreads) {
+                const uint2 v = src[i];
+                reinterpret_cast<float4*>(bcf)[i] =
+                    make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                                __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
             }
         } else {
             const float4* src = reinterpret_cast<const float4*>(st + Lay::kOffB);
