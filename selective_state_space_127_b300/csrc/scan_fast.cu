@@ -67,13 +67,39 @@ __global__ void scan_carry_kernel(float* carry, const float* sumdt, const float*
     const float a = idx_ok(d * N + n, dim * N, status) ? A[d * N + n] : 0.f;
     float H = h0 ? h0[i] : 0.f;
     carry[i] = H;
-    for (int c = 0; c < nsteps; ++c) {
-        const int64_t o = (int64_t)(c + 1) * total + i;
-        const int64_t os = (int64_t)c * batch * dim + bd;
-        if (!idx_ok(o, (int64_t)(nsteps + 1) * total, status) || !idx_ok(os, (int64_t)nsteps * batch * dim, status))
-            break;
-        H = fmaf(expf(a * sumdt[os]), H, carry[o]);
-        carry[o] = H;
+    // the local states and sums of eight chunks are loaded before any of them is combined, so
+    // eight loads are in flight instead of one (each slot is read before this thread, its only
+    // user, overwrites it)
+    constexpr int kAhead = 8;
+    for (int c0 = 0; c0 < nsteps; c0 += kAhead) {
+        float loc[kAhead], sd[kAhead];
+        bool ok = true;
+#pragma unroll
+        for (int j = 0; j < kAhead; ++j) {
+            const int c = c0 + j;
+            loc[j] = 0.f;
+            sd[j] = 0.f;
+            if (c < nsteps) {
+                const int64_t o = (int64_t)(c + 1) * total + i;
+                const int64_t os = (int64_t)c * batch * dim + bd;
+                if (idx_ok(o, (int64_t)(nsteps + 1) * total, status) &&
+                    idx_ok(os, (int64_t)nsteps * batch * dim, status)) {
+                    loc[j] = carry[o];
+                    sd[j] = sumdt[os];
+                } else {
+                    ok = false;
+                }
+            }
+        }
+        if (!ok) break;
+#pragma unroll
+        for (int j = 0; j < kAhead; ++j) {
+            const int c = c0 + j;
+            if (c < nsteps) {
+                H = fmaf(expf(a * sd[j]), H, loc[j]);
+                carry[(int64_t)(c + 1) * total + i] = H;
+            }
+        }
     }
 }
 
