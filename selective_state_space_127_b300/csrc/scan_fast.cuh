@@ -52,7 +52,10 @@ constexpr int kHalo = 3;
 // B_bar = (A_bar - 1) / A B; the sequence walked from t = L-1 down to 0 (one chunk only).
 enum Variant { kVarPlain = 0, kVarConv = 1, kVarZoh = 2, kVarRev = 3 };
 
-template <int N, bool BF16, int VAR>
+// Shared-memory layout of one CTA. HAS_Z: the z tile is loaded (the gate of the output pass);
+// READOUT: C is loaded and y staged (the output pass; the local pass needs neither, and its
+// smaller footprint lets more CTAs share an SM).
+template <int N, bool BF16, int VAR, bool HAS_Z = true, bool READOUT = true>
 struct Layout {
     static constexpr bool CONV = VAR == kVarConv;
     static constexpr int kEsz = BF16 ? 2 : 4;
@@ -62,16 +65,16 @@ struct Layout {
     static constexpr int kXBox = kXRows * kCh * kEsz;       // bytes of the x box
     static constexpr int kOffD = (kXBox + 127) / 128 * 128; // delta, z, B, C follow x
     static constexpr int kOffZ = kOffD + kTileX;
-    static constexpr int kOffB = kOffZ + kTileX;
-    static constexpr int kOffC = kOffB + kTileB;
-    static constexpr int kStageBytes = kOffC + kTileB;
+    static constexpr int kOffB = kOffZ + (HAS_Z ? kTileX : 0);
+    static constexpr int kOffC = kOffB + kTileB;                      // C right after B
+    static constexpr int kStageBytes = kOffC + (READOUT ? kTileB : 0);
     static constexpr int kStageStride = (kStageBytes + 127) / 128 * 128;
     static constexpr int kBars = 0;                                   // kStages mbarriers
     static constexpr int kRing = 128;
     static constexpr int kBCf = kRing + kStages * kStageStride;       // fp32 B then C [kT][N]
-    static constexpr int kY = kBCf + 2 * kT * N * 4;                  // 2 y tiles
-    static constexpr int kYStride = (kTileX + 127) / 128 * 128;
-    static constexpr int kTotal = kY + 2 * kYStride;
+    static constexpr int kY = kBCf + (READOUT ? 2 : 1) * kT * N * 4;  // the y tile
+    static constexpr int kYBytes = READOUT ? (kTileX + 127) / 128 * 128 : 0;
+    static constexpr int kTotal = kY + kYBytes;
 };
 
 __device__ __forceinline__ float ld_io(const void* base, int i, bool bf16) {
@@ -173,7 +176,7 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
                  const __grid_constant__ CUtensorMap mz, const __grid_constant__ CUtensorMap mB,
                  const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap my,
                  const FastParams p) {
-    using Lay = Layout<N, BF16, VAR>;
+    using Lay = Layout<N, BF16, VAR, GATE && MODE == kFull, MODE == kFull>;
     constexpr bool CONV = VAR == kVarConv;
     constexpr bool ZOH = VAR == kVarZoh;
     constexpr bool REV = VAR == kVarRev;   // one chunk only
@@ -339,8 +342,7 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
         }
         const float* Bf = bcf;
         const float* Cf = bcf + kT * N;
-        unsigned char* ys = smem + Lay::kY + (s & 1) * Lay::kYStride;
-        if (kReadout && s >= 2 && tid == 0) tma_store_wait_read<1>();   // the store of tile s-2 read ys
+        unsigned char* ys = smem + Lay::kY;
         __syncthreads();
         const int ts = REV ? ntiles - 1 - s : s;   // the tile's index in time order
         const int rem = (int)(len - (int64_t)ts * kT);
@@ -438,6 +440,10 @@ scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__
             cur = nxt;
         }
         if constexpr (kReadout) {
+            // one y tile: the store of the previous tile, committed a whole tile of updates
+            // ago, has long finished reading it
+            if (s >= 1 && tid == 0) tma_store_wait_read<0>();
+            __syncthreads();
 #pragma unroll
             for (int sg = 0; sg < kNSG; ++sg) {
                 const int j0 = rr(sg * kSG + g), j1 = rr(sg * kSG + g + LPC);
@@ -501,7 +507,7 @@ constexpr int lanes_per_channel() { return N / 8; }
 template <int N, bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS, int MODE, int VAR,
           int LPC = lanes_per_channel<N>()>
 cudaError_t launch_t(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz, cudaStream_t st) {
-    using Lay = Layout<N, BF16, VAR>;
+    using Lay = Layout<N, BF16, VAR, GATE && MODE == kFull, MODE == kFull>;
     auto kern = scan_fast_kernel<N, BF16, LPC, GATE, DSKIP, SOFTPLUS, MODE, VAR>;
     if constexpr (Lay::kTotal > 48 * 1024) {
         cudaError_t e = set_smem_once<scan_fast_kernel<N, BF16, LPC, GATE, DSKIP, SOFTPLUS, MODE, VAR>>(Lay::kTotal);
