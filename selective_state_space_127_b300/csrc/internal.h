@@ -96,6 +96,24 @@ cudaError_t set_smem_once(int bytes) {
     return e;
 }
 
+// Once per kernel and device: ask for the largest shared-memory carveout, so that as many CTAs
+// as their shared memory allows can be resident (the default carveout leaves more L1 and fewer
+// CTAs), and raise the dynamic shared-memory limit when `bytes` is above the default 48 KB.
+template <auto KERN>
+cudaError_t set_max_carveout_once(int bytes) {
+    static std::atomic<uint64_t> done{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(KERN, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess && bytes > 48 * 1024)
+        e = cudaFuncSetAttribute(KERN, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
 // Record a reason for ssm_last_error() on the calling thread; returns `s`.
 ssm_status_t set_error(ssm_status_t s, const char* msg);
 

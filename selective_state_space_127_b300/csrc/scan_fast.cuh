@@ -171,7 +171,11 @@ __device__ __forceinline__ void lds_pairs(const float* p, f2 (&v)[S / 2]) {
 }
 
 template <int N, bool BF16, int LPC, bool GATE, bool DSKIP, bool SOFTPLUS, int MODE, int VAR>
-__global__ void __launch_bounds__(kCh * LPC, 16 / LPC)
+// Registers are split between the SM's four schedulers: at most 102 per thread (96 allocated)
+// lets each hold five one-warp CTAs of the local pass (20 per SM; with 104, four: 714 against
+// 706 us on the long-sequence workload). The output pass keeps its registers: capped at 128 for
+// four CTAs per scheduler it gained 0.3 % there and lost 2.5 % on shorter, lightly loaded grids.
+__global__ void __launch_bounds__(kCh * LPC, (MODE == kPass1 && LPC == 2) ? 20 : 16 / LPC)
 scan_fast_kernel(const __grid_constant__ CUtensorMap mx, const __grid_constant__ CUtensorMap md,
                  const __grid_constant__ CUtensorMap mz, const __grid_constant__ CUtensorMap mB,
                  const __grid_constant__ CUtensorMap mC, const __grid_constant__ CUtensorMap my,
@@ -509,8 +513,9 @@ template <int N, bool BF16, bool GATE, bool DSKIP, bool SOFTPLUS, int MODE, int 
 cudaError_t launch_t(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz, cudaStream_t st) {
     using Lay = Layout<N, BF16, VAR, GATE && MODE == kFull, MODE == kFull>;
     auto kern = scan_fast_kernel<N, BF16, LPC, GATE, DSKIP, SOFTPLUS, MODE, VAR>;
-    if constexpr (Lay::kTotal > 48 * 1024) {
-        cudaError_t e = set_smem_once<scan_fast_kernel<N, BF16, LPC, GATE, DSKIP, SOFTPLUS, MODE, VAR>>(Lay::kTotal);
+    {
+        cudaError_t e = set_max_carveout_once<scan_fast_kernel<N, BF16, LPC, GATE, DSKIP, SOFTPLUS, MODE, VAR>>(
+            Lay::kTotal);
         if (e != cudaSuccess) return e;
     }
     dim3 grid((unsigned)((a.dim + kCh - 1) / kCh), (unsigned)a.batch, (unsigned)nz);
