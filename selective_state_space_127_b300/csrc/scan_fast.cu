@@ -11,8 +11,10 @@
 //
 // Data movement. TMA (3-D tensor maps over (D or N, L, b)) streams 32-step tiles of x,
 // delta, z, B and C into a 2-deep shared-memory ring guarded by mbarriers; y tiles leave
-// through TMA stores from a double buffer. B and C tiles are widened to fp32 once per tile
-// by the CTA, so lanes then read their states' values with 8- or 16-byte loads.
+// through TMA stores from one staging tile (the store of a tile has long finished reading it
+// when the next tile's outputs are written). B and C tiles are widened to fp32 once per tile
+// by the CTA, so lanes then read their states' values with 8- or 16-byte loads. The local pass
+// loads neither z nor C and stages no y, so its CTAs take about half the shared memory.
 //
 // Steps go in supergroups of 2 LPC. Lane g of a channel computes the per-(t, channel) scalars
 // of steps g and g + LPC of the supergroup (dt = softplus(delta + bias), dt x, silu(z), D x)
