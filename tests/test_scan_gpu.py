@@ -238,10 +238,11 @@ def test_host_entry_point_pipelines_rows_and_matches_device_call(cuda_dev, slice
         assert torch.equal(h, h_ref.cpu())
 
 
-@pytest.mark.parametrize("segments,reverse,conv,batch", [(1, False, False, 1), (3, False, False, 1),
-                                                        (8, False, False, 2), (5, True, False, 1),
-                                                        (4, False, True, 1), (6, False, True, 3)])
-def test_host_entry_point_pipelines_sequence_stretches(cuda_dev, segments, reverse, conv, batch):
+@pytest.mark.parametrize("segments,reverse,conv,batch,zoh", [(1, False, False, 1, False), (3, False, False, 1, False),
+                                                            (8, False, False, 2, False), (5, True, False, 1, False),
+                                                            (4, False, True, 1, False), (6, False, True, 3, False),
+                                                            (7, False, False, 1, True), (3, True, False, 2, True)])
+def test_host_entry_point_pipelines_sequence_stretches(cuda_dev, segments, reverse, conv, batch, zoh):
     """With fewer rows than slices, ssm_scan_fwd_host cuts the sequence into stretches scanned
     in order, each from the state the previous one left (and, with the conv prologue, the raw
     inputs before it). With one chunk per call the arithmetic of every step is that of the
@@ -250,7 +251,7 @@ def test_host_entry_point_pipelines_sequence_stretches(cuda_dev, segments, rever
     inp = make_scan_inputs(batch, L, Dm, 16, "bf16", seed=55, d_skip="normal", gate=True)
     gen = torch.Generator().manual_seed(56)
     inp["h0"] = torch.randn(batch, Dm, 16, generator=gen)
-    kw = dict(chunk_len=1024, reverse=reverse)
+    kw = dict(chunk_len=1024, reverse=reverse, zoh=zoh)
     if conv:
         inp["conv_weight"] = torch.randn(Dm, 4, generator=gen) * 0.5
         inp["conv_bias"] = torch.randn(Dm, generator=gen) * 0.1
