@@ -594,15 +594,19 @@ def run_ours(args):
                            "vs_plain_scan": round(fms / ms1, 3) if ms1 else None}}
 
     if not args.no_variants:
-        # the exact-ZOH discretisation and the reverse direction on workload 1 (TMA kernel variants)
+        # the exact-ZOH discretisation and the reverse direction on workload 1 (TMA kernel variants),
+        # and the in-tile associative scan (the other algorithm of the same call)
         variants = {}
-        for name, kw in (("zoh", {"zoh": True}), ("reverse", {"reverse": True})):
+        kernel_of = {"zoh": "scan_fast_kernel (zoh variant)", "reverse": "scan_fast_kernel (reverse variant)",
+                     "assoc_scan": "scan_assoc_kernel (algorithm=assoc)"}
+        for name, kw in (("zoh", {"zoh": True}), ("reverse", {"reverse": True}),
+                         ("assoc_scan", {"algorithm": "assoc"})):
             def vstep(kw=kw):
                 ssm_scan_fwd(**inp1, out=y1, h_last=hl1, workspace=ws1, **kw)
             vms = _max_over_ranks(_timed(vstep, few, 3, stream, barrier), dev, world)
             variants[name] = {"ms_per_step": round(vms, 4), "gbs": round(nbytes1 / (vms * 1e-3) / 1e9 * world, 1),
                               "vs_plain_scan": round(vms / ms1, 3) if ms1 else None,
-                              "kernel": f"scan_fast_kernel ({name} variant)"}
+                              "kernel": kernel_of[name]}
         result["variants"] = dict(workload=w1.name, **variants)
 
     if not args.no_decode:

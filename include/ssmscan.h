@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define SSMSCAN_ABI_VERSION 3
+#define SSMSCAN_ABI_VERSION 4
 
 /* Bytes at the start of every workspace that hold the device status word (a uint32 at offset 0;
  * the rest is reserved). */
@@ -77,6 +77,17 @@ typedef enum { SSM_DTYPE_F32 = 0, SSM_DTYPE_BF16 = 1 } ssm_dtype_t;
  *   ("State Space Model / Mamba", "Zero-Order Hold" and `discretize_zoh`; "Mamba/SSM
  *   complete guide" section 2 ZOH formula), with the limit delta * B where a == 0. */
 typedef enum { SSM_DISC_DELTA_B = 0, SSM_DISC_ZOH = 1 } ssm_discretization_t;
+
+/* How the recurrence walks the sequence inside a chunk (ssm_scan_params.algorithm); both give
+ * the same result up to fp32 rounding.
+ *  SSM_SCAN_ALGO_SERIAL (default): each lane walks its states' steps one after the other.
+ *  SSM_SCAN_ALGO_ASSOC: each warp runs an inclusive scan of the (A_bar, B_bar x) pairs of a
+ *    32-step tile over its lanes with the operator (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2)
+ *    ("Mamba/SSM complete guide" section 5 `parallel_scan`), tiles joined through the state.
+ *    About ten times slower on B300 (eleven shuffles per state and step); N = 16 or 32,
+ *    forward, delta B, no conv prologue, and the TMA layout (dense channel-contiguous rows,
+ *    16-byte aligned); anything else is SSM_ERR_UNSUPPORTED. */
+typedef enum { SSM_SCAN_ALGO_SERIAL = 0, SSM_SCAN_ALGO_ASSOC = 1 } ssm_scan_algo_t;
 
 /* Test hooks (debug_flags). SSM_DEBUG_SKIP_FIRST_LOAD: the TMA path never issues the copy
  * of its first tile, so its bounded wait runs out (about one second), the kernel latches
@@ -160,7 +171,7 @@ typedef struct ssm_scan_params {
                                  too (the long-sequence path launches 3 kernels: local pass, chunk
                                  carry, output pass; the others 1) */
     int32_t n_phase_events;   /* entries of phase_events (0 when it is NULL) */
-    int32_t reserved3;        /* must be 0 */
+    int32_t algorithm;        /* ssm_scan_algo_t: SSM_SCAN_ALGO_SERIAL (0) unless chosen */
 } ssm_scan_params;
 
 /* Bytes of device workspace ssm_scan_fwd needs for these params: 0 for the paths without

@@ -23,7 +23,7 @@ SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT,
     range(7)
 SSM_DTYPE_F32, SSM_DTYPE_BF16 = 0, 1
 SSM_DISC_DELTA_B, SSM_DISC_ZOH = 0, 1
-ABI_VERSION = 3
+ABI_VERSION = 4
 WORKSPACE_HEADER_BYTES = 256   # SSM_WORKSPACE_HEADER_BYTES: the status word of a workspace
 
 # Every function the header declares (checked by the CPU test suite).
@@ -46,7 +46,7 @@ class ScanParams(ctypes.Structure):
                 ("debug_flags", _i32), ("reserved", _i32),
                 ("conv_weight", _vp), ("conv_bias", _vp), ("conv_x_prev", _vp), ("conv_width", _i32),
                 ("reserved2", _i32), ("phase_events", ctypes.POINTER(_vp)), ("n_phase_events", _i32),
-                ("reserved3", _i32)]
+                ("algorithm", _i32)]
 
 
 class Conv1dParams(ctypes.Structure):
@@ -185,9 +185,15 @@ def _event_array(events):
     return arr, len(handles)
 
 
+# ssm_scan_params.algorithm: the serial walk (default) or the in-tile associative scan
+SSM_SCAN_ALGO_SERIAL, SSM_SCAN_ALGO_ASSOC = 0, 1
+_ALGOS = {"serial": SSM_SCAN_ALGO_SERIAL, "assoc": SSM_SCAN_ALGO_ASSOC}
+
+
 def _scan_params(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_softplus=True, h0=None,
                  reverse=False, zoh=False, chunk_len=0, out=None, return_last_state=True, h_last=None,
-                 debug_flags=0, conv_weight=None, conv_bias=None, conv_x_prev=None, phase_events=None):
+                 debug_flags=0, conv_weight=None, conv_bias=None, conv_x_prev=None, phase_events=None,
+                 algorithm="serial"):
     """Check the tensors and fill a ScanParams; returns (params, y, h_last)."""
     if not x.is_cuda:
         raise ValueError("x must be a CUDA tensor (use ssm_scan_fwd_host for host buffers)")
@@ -236,6 +242,9 @@ def _scan_params(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_so
     p.C_stride[:] = _strides3(C)
     p.chunk_len = int(chunk_len)
     p.debug_flags = int(debug_flags)
+    if algorithm not in _ALGOS:
+        raise ValueError(f"algorithm must be one of {sorted(_ALGOS)}")
+    p.algorithm = _ALGOS[algorithm]
     if conv_weight is not None:
         p.conv_weight, p.conv_bias, p.conv_x_prev = _ptr(conv_weight), _ptr(conv_bias), _ptr(conv_x_prev)
         p.conv_width = K
@@ -260,7 +269,7 @@ def scan_workspace_size(x, delta, A, B, C, D=None, z=None, delta_bias=None, **kw
 def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_softplus=True, h0=None,
                  reverse=False, zoh=False, chunk_len=0, out=None, return_last_state=True, h_last=None,
                  stream=None, workspace=None, debug_flags=0, conv_weight=None, conv_bias=None, conv_x_prev=None,
-                 phase_events=None):
+                 phase_events=None, algorithm="serial"):
     """Selective scan on the GPU. x, delta, z: (b, L, D); B, C: (b, L, N); A: (D, N) fp32;
     D, delta_bias: (D) fp32; h0: (b, D, N) fp32. I/O tensors are fp32 or bf16 (all alike) and
     may be strided (delta's channel stride may be 0). ``workspace`` (a uint8 CUDA tensor of at
@@ -270,13 +279,16 @@ def ssm_scan_fwd(x, delta, A, B, C, D=None, z=None, delta_bias=None, *, delta_so
     With ``conv_weight`` (D, K) fp32 (K <= 4), x is the raw input and the scan runs on
     silu(causal conv1d(x) + conv_bias); ``conv_x_prev`` (b, K-1, D) holds the K-1 raw inputs
     before x[:, 0] (zeros when None). ``phase_events``: torch.cuda.Event objects recorded
-    before the call's first kernel and after each kernel. Returns (y, h_last or None)."""
+    before the call's first kernel and after each kernel. ``algorithm``: "serial" (default:
+    each lane walks its states' steps) or "assoc" (an in-tile associative scan of the
+    (A_bar, B_bar x) pairs over a warp's lanes; N = 16 or 32, forward, delta B, TMA layout).
+    Returns (y, h_last or None)."""
     lib = load_library()
     p, y, hl = _scan_params(x, delta, A, B, C, D, z, delta_bias, delta_softplus=delta_softplus, h0=h0,
                             reverse=reverse, zoh=zoh, chunk_len=chunk_len, out=out,
                             return_last_state=return_last_state, h_last=h_last, debug_flags=debug_flags,
                             conv_weight=conv_weight, conv_bias=conv_bias, conv_x_prev=conv_x_prev,
-                            phase_events=phase_events)
+                            phase_events=phase_events, algorithm=algorithm)
     ws_bytes = lib.ssm_scan_workspace_size(ctypes.byref(p))
     if ws_bytes == ctypes.c_size_t(-1).value:
         _check(lib, lib.ssm_scan_fwd(ctypes.byref(p), None))  # raises with the reason

@@ -114,9 +114,14 @@ ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
     if ((p->delta_softplus != 0 && p->delta_softplus != 1) || (p->reverse != 0 && p->reverse != 1))
         return fail(SSM_ERR_INVALID_ARG, "delta_softplus and reverse must be 0 or 1");
     if (p->chunk_len < 0) return fail(SSM_ERR_INVALID_ARG, "chunk_len must be >= 0");
-    if (p->reserved != 0 || p->reserved2 != 0 || p->reserved3 != 0 ||
-        (p->debug_flags & ~SSM_DEBUG_SKIP_FIRST_LOAD) != 0)
+    if (p->reserved != 0 || p->reserved2 != 0 || (p->debug_flags & ~SSM_DEBUG_SKIP_FIRST_LOAD) != 0)
         return fail(SSM_ERR_INVALID_ARG, "unknown debug_flags or nonzero reserved field");
+    if (p->algorithm != SSM_SCAN_ALGO_SERIAL && p->algorithm != SSM_SCAN_ALGO_ASSOC)
+        return fail(SSM_ERR_INVALID_ARG, "algorithm %d unknown", p->algorithm);
+    if (p->algorithm == SSM_SCAN_ALGO_ASSOC &&
+        (p->reverse || p->discretization != SSM_DISC_DELTA_B || p->conv_weight || (p->dstate != 16 && p->dstate != 32)))
+        return fail(SSM_ERR_UNSUPPORTED,
+                    "the associative scan takes N = 16 or 32, forward, delta B, no conv prologue");
     if (p->n_phase_events < 0 || p->n_phase_events > kMaxPhaseEvents || (p->n_phase_events > 0) != (p->phase_events != nullptr))
         return fail(SSM_ERR_INVALID_ARG, "phase_events must be NULL with n_phase_events == 0, or hold 1..%d events",
                     kMaxPhaseEvents);
@@ -204,6 +209,7 @@ ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
     a.workspace = p->workspace;
     a.workspace_bytes = p->workspace_bytes;
     a.debug_flags = p->debug_flags;
+    a.algorithm = p->algorithm;
     a.conv_w = p->conv_weight;
     a.conv_b = p->conv_weight ? p->conv_bias : nullptr;
     a.conv_prev = p->conv_weight ? p->conv_x_prev : nullptr;
@@ -224,6 +230,9 @@ ssm_status_t validate_scan(const ssm_scan_params* p, ssm::ScanArgs* out) {
     a.ext_y = ext(act, p->y_stride);
     a.ext_B = ext(bc, p->B_stride);
     a.ext_C = ext(bc, p->C_stride);
+    if (a.algorithm == SSM_SCAN_ALGO_ASSOC && a.seqlen > 0 && !ssm::scan_fast_supported(a))
+        return fail(SSM_ERR_UNSUPPORTED, "the associative scan needs the TMA layout (dense channel-contiguous "
+                                         "rows, 16-byte aligned) and a driver");
     return SSM_OK;
 }
 
@@ -289,8 +298,13 @@ constexpr bool kStatusEverywhere = false;
 // The TMA kernels wait (bounded) on their copies, so they need the status header; the split
 // sequence adds its chunk carries after it. The short-sequence and generic kernels need none
 // (except in the debug build).
+bool takes_tma_path(const ssm::ScanArgs& a) {
+    if (a.algorithm == SSM_SCAN_ALGO_ASSOC) return a.seqlen > 0;   // validated: TMA layout
+    return a.seqlen > kShortSeq && ssm::scan_fast_supported(a);
+}
+
 size_t scan_workspace_bytes(const ssm::ScanArgs& a) {
-    if (a.seqlen <= kShortSeq || !ssm::scan_fast_supported(a))
+    if (!takes_tma_path(a))
         return kStatusEverywhere && a.seqlen > 0 ? SSM_WORKSPACE_HEADER_BYTES : 0;
     return SSM_WORKSPACE_HEADER_BYTES + ssm::scan_fast_workspace_bytes(a);
 }
@@ -401,7 +415,7 @@ ssm_status_t ssm_scan_fwd(const ssm_scan_params* p, void* stream) {
         (a.seqlen <= kShortSeq || a.seqlen > 16 || !ssm::scan_fast_supported(a)))
         return fail(SSM_ERR_INVALID_ARG, "SSM_DEBUG_SKIP_FIRST_LOAD needs %lld < seqlen <= 16 and the TMA path",
                     (long long)kShortSeq);
-    if (a.seqlen > kShortSeq && ssm::scan_fast_supported(a)) {
+    if (takes_tma_path(a)) {
         e = ssm::launch_scan_fast(a, st);   // records its own phase events
     } else {
         e = ssm::record_phase(a, 0, false, st);

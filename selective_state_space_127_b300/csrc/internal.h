@@ -32,6 +32,7 @@ struct ScanArgs {
     void* workspace;
     size_t workspace_bytes;
     int debug_flags;
+    int algorithm;           // SSM_SCAN_ALGO_SERIAL or SSM_SCAN_ALGO_ASSOC
     // causal conv1d + SiLU prologue on x (conv_w == nullptr: none)
     const float* conv_w;     // (D, K)
     const float* conv_b;     // (D) or nullptr

@@ -207,6 +207,7 @@ cudaError_t launch_scan_fast(const ScanArgs& a, cudaStream_t st) {
     const void* zsrc = a.z ? a.z : a.x;                 // unused map when there is no gate
     const int64_t* zst = a.z ? a.zs : a.xs;
     const bool conv = a.conv_w != nullptr;
+    const bool assoc = a.algorithm == SSM_SCAN_ALGO_ASSOC;
     if (!make_map(&maps[0], a.x, bf, a.dim, a.seqlen, a.batch, a.xs[1], a.xs[0], kCh, conv ? kT + kHalo : kT) ||
         !make_map(&maps[1], a.delta, bf, a.dim, a.seqlen, a.batch, a.ds[1], a.ds[0], kCh) ||
         !make_map(&maps[2], zsrc, bf, a.dim, a.seqlen, a.batch, zst[1], zst[0], kCh) ||
@@ -227,9 +228,10 @@ cudaError_t launch_scan_fast(const ScanArgs& a, cudaStream_t st) {
         const size_t slot_floats = (size_t)(a.batch * a.dim * a.dstate);
         fp.carry = reinterpret_cast<float*>(static_cast<unsigned char*>(a.workspace) + SSM_WORKSPACE_HEADER_BYTES);
         fp.sumdt = fp.carry + (size_t)nch * slot_floats;
-        e = conv     ? dispatch_conv_pass1(maps, fp, a, nch - 1, st)
-            : a.zoh ? dispatch_zoh_pass1(maps, fp, a, nch - 1, st)
-                    : dispatch<kPass1, kVarPlain>(maps, fp, a, nch - 1, st);
+        e = assoc    ? dispatch_assoc_pass1(maps, fp, a, nch - 1, st)
+            : conv   ? dispatch_conv_pass1(maps, fp, a, nch - 1, st)
+            : a.zoh  ? dispatch_zoh_pass1(maps, fp, a, nch - 1, st)
+                     : dispatch<kPass1, kVarPlain>(maps, fp, a, nch - 1, st);
         if (e == cudaSuccess) e = record_phase(a, 1, false, st);
         if (e != cudaSuccess) return e;
         const int64_t total = a.batch * a.dim * a.dstate;
@@ -240,7 +242,8 @@ cudaError_t launch_scan_fast(const ScanArgs& a, cudaStream_t st) {
         if (e == cudaSuccess) e = record_phase(a, 2, false, st);
         if (e != cudaSuccess) return e;
     }
-    e = conv     ? dispatch_conv_full(maps, fp, a, nch, st)
+    e = assoc    ? dispatch_assoc_full(maps, fp, a, nch, st)
+        : conv   ? dispatch_conv_full(maps, fp, a, nch, st)
         : a.zoh ? dispatch_zoh_full(maps, fp, a, nch, st)
         : a.reverse ? dispatch_rev_full(maps, fp, a, nch, st)
                     : dispatch<kFull, kVarPlain>(maps, fp, a, nch, st);

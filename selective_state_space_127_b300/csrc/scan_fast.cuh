@@ -573,6 +573,11 @@ cudaError_t dispatch_zoh_pass1(const CUtensorMap* maps, const FastParams& fp, co
                                cudaStream_t st);
 cudaError_t dispatch_rev_full(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz,
                               cudaStream_t st);
+// The in-tile associative scan (scan_assoc.cu), N in {16, 32}, forward, delta B.
+cudaError_t dispatch_assoc_full(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz,
+                                cudaStream_t st);
+cudaError_t dispatch_assoc_pass1(const CUtensorMap* maps, const FastParams& fp, const ScanArgs& a, int nz,
+                                 cudaStream_t st);
 
 }  // namespace fast
 }  // namespace ssm

@@ -149,8 +149,22 @@ def test_phase_event_fields_are_checked(lib):
     p.n_phase_events = 2                  # no array
     assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
     p = _valid_scan_params()
-    p.reserved3 = 1
+    p.reserved2 = 1
     assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
+
+
+def test_algorithm_field_is_checked(lib):
+    """algorithm: 0 (serial walk) or 1 (in-tile associative scan); anything else is an argument
+    error, and the associative scan refuses what it does not take before any launch."""
+    p = _valid_scan_params()
+    p.algorithm = 2
+    assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_INVALID_ARG
+    assert lib.ssm_scan_workspace_size(ctypes.byref(p)) == ctypes.c_size_t(-1).value
+    for field, value in (("reverse", 1), ("discretization", binding.SSM_DISC_ZOH), ("dstate", 64)):
+        p = _valid_scan_params()
+        p.algorithm = binding.SSM_SCAN_ALGO_ASSOC
+        setattr(p, field, value)
+        assert lib.ssm_scan_fwd(ctypes.byref(p), None) == binding.SSM_ERR_UNSUPPORTED, field
 
 
 def test_workspace_sizes_include_the_status_header(lib):
