@@ -20,6 +20,14 @@ constexpr int kDecodeThreads = 256;
 
 template <int TPC>
 __global__ void __launch_bounds__(kDecodeThreads) scan_decode_kernel(const ScanArgs a) {
+    // Programmatic dependent launch: this grid may have started before the kernel ahead of it on
+    // the stream finished (a decode loop's previous token, which wrote the state). Wait for that
+    // grid's memory operations before the first global access, then let the next kernel's launch
+    // begin while this one runs (it waits in turn). Without a programmatic predecessor the wait
+    // returns at once. (Releasing the next launch before the wait, so that launches run two
+    // steps ahead, measured 2.54 against 2.38 us per token.)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t gtid = (int64_t)blockIdx.x * kDecodeThreads + threadIdx.x;
     const int64_t chan = gtid / TPC;
     const int g = (int)(gtid % TPC);
@@ -94,9 +102,20 @@ cudaError_t launch(const ScanArgs& a, cudaStream_t st) {
     const int64_t threads = a.batch * a.dim * TPC;
     const int64_t grid = (threads + kDecodeThreads - 1) / kDecodeThreads;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
-    scan_decode_kernel<TPC><<<(unsigned)grid, kDecodeThreads, 0, st>>>(a);
+    // launched as a programmatic dependent of the previous kernel on the stream (see the kernel)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kDecodeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, scan_decode_kernel<TPC>, a);
     note_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
