@@ -200,7 +200,119 @@ class ClockSampler:
         watts = [num(r[1][2]) for r in rows if num(r[1][2]) is not None]
         return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
                 "power_w_max": max(watts) if watts else None, "samples": len(rows), "in_window": in_window,
-                "reasons": reasons}
+                "reasons": reasons, "source": "nvidia-smi, 100 ms",
+                **({"nvml_unused": self.nvml_error} if getattr(self, "nvml_error", None) else {})}
+
+
+class _NvmlLib:
+    """The few read-only NVML calls the clock record needs, through ctypes on the driver's
+    libnvidia-ml (no Python bindings needed)."""
+    CLOCK_SM = 1
+
+    def __init__(self):
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self._ok(self.lib.nvmlInit_v2())
+        f = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self._reasons = f if f is not None else self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    @staticmethod
+    def _ok(r):
+        if r != 0:
+            raise RuntimeError(f"NVML error {r}")
+
+    def handle(self, uuid, index):
+        h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+            self._ok(self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h)))
+        return h
+
+    def sm_mhz(self, h):
+        v = ctypes.c_uint()
+        self._ok(self.lib.nvmlDeviceGetClockInfo(h, self.CLOCK_SM, ctypes.byref(v)))
+        return v.value
+
+    def max_sm_mhz(self, h):
+        v = ctypes.c_uint()
+        self._ok(self.lib.nvmlDeviceGetMaxClockInfo(h, self.CLOCK_SM, ctypes.byref(v)))
+        return v.value
+
+    def watts(self, h):
+        v = ctypes.c_uint()
+        self._ok(self.lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(v)))
+        return v.value / 1000.0
+
+    def reasons(self, h):
+        v = ctypes.c_ulonglong()
+        self._ok(self._reasons(h, ctypes.byref(v)))
+        return v.value
+
+    def shutdown(self):
+        self.lib.nvmlShutdown()
+
+
+class NvmlClockSampler:
+    """The same record as ClockSampler from NVML (read-only queries: SM clock, maximum SM clock,
+    power draw, active clock-event reasons) every 5 ms in a thread, so that a timed region of a
+    few tens of milliseconds still holds several samples."""
+
+    # clock-event reason bits of NVML's public header
+    BITS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40), ("sw_thermal_slowdown", 0x20),
+            ("sw_power_cap", 0x4))
+
+    def __init__(self, device_index, period_s=0.005):
+        import torch
+        self.nv = _NvmlLib()
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+        visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+        self.h = self.nv.handle(uuid, int(visible.split(",")[device_index]) if visible and
+                                visible.split(",")[device_index].isdigit() else device_index)
+        self.max_mhz = self.nv.max_sm_mhz(self.h)
+        self.rows, self.window, self.period = [], None, period_s
+        self.done = threading.Event()
+        self.t = threading.Thread(target=self._run, daemon=True)
+        self.t.start()
+
+    def _run(self):
+        while not self.done.is_set():
+            try:
+                self.rows.append((time.time(), self.nv.sm_mhz(self.h), self.nv.watts(self.h),
+                                  self.nv.reasons(self.h)))
+            except Exception:
+                pass
+            self.done.wait(self.period)
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        self.done.set()
+        self.t.join(timeout=5)
+        try:
+            self.nv.shutdown()
+        except Exception:
+            pass
+
+    def summary(self):
+        rows, in_window = self.rows, False
+        if self.window:
+            inside = [r for r in rows if self.window[0] <= r[0] <= self.window[1]]
+            if inside:
+                rows, in_window = inside, True
+        reasons = sorted({name for r in rows for name, bit in self.BITS if r[3] & bit})
+        mhz = [r[1] for r in rows]
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(r[2] for r in rows) if rows else None, "samples": len(rows),
+                "in_window": in_window, "reasons": reasons, "source": "nvml, 5 ms"}
+
+
+def clock_sampler(device_index):
+    """NVML sampling when the NVML bindings load, else nvidia-smi (the reason is recorded)."""
+    try:
+        return NvmlClockSampler(device_index)
+    except Exception as e:
+        c = ClockSampler(device_index)
+        c.nvml_error = f"{type(e).__name__}: {e}"[:200]
+        return c
 
 
 # ------------------------------------------------------------------ oracle timing (CPU)
@@ -471,7 +583,7 @@ def run_ours(args):
     binding.load_library()
     peaks, peak_src = load_peaks()
     stream = torch.cuda.current_stream()
-    clk = ClockSampler(local)
+    clk = clock_sampler(local)
     few = max(3, min(args.steps, 20))
 
     # the other scan workloads first (they also bring the GPU to its working clock)
