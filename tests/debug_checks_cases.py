@@ -46,6 +46,9 @@ def run(dev):
     inp = _to(dev, make_scan_inputs(2, 700, 40, 16, "bf16", seed=71, d_skip="normal"))
     state = torch.randn(2, 40, 16, generator=g).to(dev)
     scan("split_in_place", inp, h0=state, h_last=state, chunk_len=64)
+    h0a = torch.randn(2, 40, 32, generator=torch.Generator().manual_seed(2)).to(dev)
+    scan("assoc_split", _to(dev, make_scan_inputs(2, 700, 40, 32, "bf16", seed=78)), h0=h0a, chunk_len=96,
+         algorithm="assoc")
     scan("reverse_f32", _to(dev, make_scan_inputs(1, 300, 48, 32, "f32", seed=72)), reverse=True)
     cw, cb = (torch.randn(32, 4, generator=g) / 2).to(dev), (0.1 * torch.randn(32, generator=g)).to(dev)
     inp = _to(dev, make_scan_inputs(2, 200, 32, 16, "bf16", seed=73))
