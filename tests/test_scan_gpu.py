@@ -266,6 +266,19 @@ def test_host_entry_point_pipelines_sequence_stretches(cuda_dev, segments, rever
         assert torch.equal(h, h_ref.cpu())
 
 
+def test_host_entry_point_stretches_with_chunks_match_oracle(cuda_dev):
+    """The shape of the end-to-end bench: one batch row cut into eight stretches, each split into
+    chunks joined by the carry kernel with h0 and h_last one buffer; against the oracle."""
+    L, Dm = 16384, 64
+    inp = make_scan_inputs(1, L, Dm, 16, "bf16", seed=91, d_skip="normal", gate=True)
+    h0 = torch.randn(1, Dm, 16, generator=torch.Generator().manual_seed(92))
+    host = {k: (v.pin_memory() if v is not None else None) for k, v in dict(inp, h0=h0).items()}
+    y, h = binding.ssm_scan_fwd_host(host, device=cuda_dev, dev_buffers={}, segments=8, chunk_len=1024)
+    y_ref, h_ref = oracle.ssm_scan_ref(**inp, h0=h0)
+    assert rel_l2(y.float().numpy(), y_ref) <= TOL_Y["bf16"]
+    assert rel_l2(h.numpy(), h_ref) <= TOL_H["bf16"]
+
+
 @pytest.mark.parametrize("dt", ["f32", "bf16"])
 def test_decode_steps_advance_the_state_in_place(cuda_dev, dt):
     """Single-token recurrent inference: T calls with L = 1 and h0 = h_last = one state buffer
