@@ -1,6 +1,6 @@
-"""Seeded random configurations of the selective scan (shapes, dtypes and every optional
-feature together) against the fp64 oracle, so that combinations the targeted tests do not name
-are exercised on whichever kernel the library picks for them."""
+"""Seeded random configurations of the selective scan (shapes, dtypes, both algorithms, strided
+inputs and every optional feature together) against the fp64 oracle, so that combinations the
+targeted tests do not name are exercised on whichever kernel the library picks for them."""
 import random
 
 import pytest
@@ -35,10 +35,13 @@ def _config(i):
     cfg["zoh"] = variant == "zoh"
     cfg["reverse"] = variant == "reverse"
     cfg["conv"] = r.choice([2, 3, 4]) if variant == "conv" else 0
+    # drawn last, so the earlier fields of configuration i stay what they were
+    cfg["algorithm"] = "assoc" if variant == "plain" and cfg["N"] in (16, 32) and r.random() < 0.3 else "serial"
+    cfg["strided_x"] = cfg["algorithm"] == "serial" and r.random() < 0.2   # the generic kernel
     return cfg
 
 
-@pytest.mark.parametrize("i", range(40))
+@pytest.mark.parametrize("i", range(120))
 def test_random_configuration_matches_oracle(cuda_dev, i):
     c = _config(i)
     inp = make_scan_inputs(c["b"], c["L"], c["D"], c["N"], c["dt"], seed=9100 + i,
@@ -48,7 +51,8 @@ def test_random_configuration_matches_oracle(cuda_dev, i):
         inp["delta_bias"] = torch.full_like(inp["delta_bias"], 1e-3)
     g = torch.Generator().manual_seed(9200 + i)
     h0 = torch.randn(c["b"], c["D"], c["N"], generator=g) if c["h0"] else None
-    kw = dict(delta_softplus=c["softplus"], zoh=c["zoh"], reverse=c["reverse"], chunk_len=c["chunk"])
+    kw = dict(delta_softplus=c["softplus"], zoh=c["zoh"], reverse=c["reverse"], chunk_len=c["chunk"],
+              algorithm=c["algorithm"])
     conv = {}
     x_ref = inp["x"]
     if c["conv"]:
@@ -57,6 +61,11 @@ def test_random_configuration_matches_oracle(cuda_dev, i):
         conv = dict(conv_weight=w.to(cuda_dev), conv_bias=cb.to(cuda_dev))
         x_ref = oracle.causal_conv1d_ref(inp["x"], w, cb)
     dev_inp = {k: (v.to(cuda_dev) if v is not None else None) for k, v in inp.items()}
+    if c["strided_x"]:   # x as a view with a row stride of D + 3 elements
+        x = dev_inp["x"]
+        wide = torch.zeros(x.shape[0], x.shape[1], x.shape[2] + 3, dtype=x.dtype, device=cuda_dev)
+        wide[..., :x.shape[2]] = x
+        dev_inp["x"] = wide[..., :x.shape[2]]
     h0_d = h0.to(cuda_dev) if h0 is not None else None
     ws = new_workspace(binding.scan_workspace_size(**dev_inp, h0=h0_d, **kw, **conv), cuda_dev)
     y, h = ssm_scan_fwd(**dev_inp, h0=h0_d, workspace=ws, **kw, **conv)
